@@ -1,0 +1,574 @@
+"""Pins of the CPU oracle to facts other than its own code (no GPU).
+
+Each test checks the oracle against something the page or the mathematics
+fixes: hand-worked examples (tests/golden), the functional equivalence the
+page rests on ("one model, two layouts": EP and TP compute the same function on
+the same bytes, "Moebius: Serving Mixture-of-Expert Models with Seamless
+Runtime Parallelism Switch" (paper review) §3), round trips, exactly-once and
+replication counts, special cases that reduce to numpy/torch slicing, the
+byte accounting of §4.3 Table 1, the layer order of §4.2 Fig. 7, and brute
+force for the greedy placement of §3.2.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (bf16_to_f64, dims_of, fill_regions, gather_tokens, heads_of_rank,
+                     initial_kv_state, ints, kv_ep, kv_tp, read_golden, w13_ep, w13_tp,
+                     w2_ep, w2_tp, wslot)
+from synth.workloads import TINY, Workload
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+SMALL_W = Workload("w_small", P=4, N=3, E=8, H=24, I=16, w_sigma=0.5)
+SMALL_KV = Workload("kv_small", P=4, N=3, Hkv=2, D=8, ps=4, R=9, len_kind="uniform",
+                    len_a=1, len_b=23, kv_sigma=1.0)
+
+
+# ----------------------------------------------------------------------------- layout
+
+@pytest.mark.parametrize("w", [TINY, SMALL_W, SMALL_KV, TINY.with_(Hkv=4, P=2, E=4)])
+def test_layout_parts_disjoint_and_aligned(w):
+    d = dims_of(w)
+    L = oracle.layout(d)
+    El, Ip = d.E // d.P, d.I // d.P
+    w13 = El * 2 * d.I * d.H * 2
+    w2 = El * d.H * d.I * 2
+    assert L["w2_off"] >= w13 and L["w2_off"] % 256 == 0
+    if d.E:
+        assert L["wslot_stride"] >= L["w2_off"] + w2 and L["wslot_stride"] % 4096 == 0
+    # the same bytes per slot in both views (§3: only ownership changes)
+    assert w13 == d.E * 2 * Ip * d.H * 2 and w2 == d.E * d.H * Ip * 2
+    if d.Hkv:
+        half_tp = L["pages_tp"] * d.ps * L["h_tp"] * d.D * 2
+        half_ep = L["pages_ep"] * d.ps * d.Hkv * d.D * 2
+        assert half_ep == half_tp
+        assert L["kv_v_off"] >= half_tp and L["kv_v_off"] % 256 == 0
+        assert L["kvslot_stride"] >= L["kv_v_off"] + half_tp
+    assert L["kvslots_off"] == (d.N + 1) * L["wslot_stride"]
+    assert L["region_stride"] >= (d.N + 1) * (L["wslot_stride"] + L["kvslot_stride"])
+    assert L["region_stride"] % (2 << 20) == 0
+    assert L["ws_off"] == d.P * L["region_stride"]
+
+
+# ----------------------------------------------------------------------------- weights
+
+def _tagged_weights(d: oracle.Dims, L: dict, tag_w13, tag_w2, slot: int) -> np.ndarray:
+    buf = np.zeros(L["ws_off"], dtype=np.uint8)
+    for r in range(d.P):
+        a = w13_ep(buf, L, d, r, slot)
+        b = w2_ep(buf, L, d, r, slot)
+        for el in range(d.E // d.P):
+            e = r * (d.E // d.P) + el
+            for j in range(2 * d.I):
+                for h in range(d.H):
+                    a[el, j, h] = tag_w13(e, j, h)
+            for h in range(d.H):
+                for i in range(d.I):
+                    b[el, h, i] = tag_w2(e, h, i)
+    return buf
+
+
+def test_weights_golden_hand_worked():
+    g = read_golden("w13_w2_p2_e2_h2_i4.txt")
+    kv = {ln.split()[0]: int(ln.split()[1]) for ln in g if ln.split()[0] in ("P", "E", "H", "I")}
+    d = oracle.Dims(P=kv["P"], E=kv["E"], H=kv["H"], I=kv["I"], N=1)
+    L = oracle.layout(d)
+    buf = _tagged_weights(d, L, lambda e, j, h: 100 * e + 10 * j + h,
+                          lambda e, h, i: 1000 + 100 * e + 10 * h + i, slot=1)
+    oracle.weights_ep2tp(buf, d)
+    n = 0
+    for ln in g:
+        name, rest = ln.split(" ", 1)
+        if name not in ("tp_w13", "tp_w2"):
+            continue
+        head, vals = rest.split(":")
+        q, e = ints(head)
+        got = (w13_tp if name == "tp_w13" else w2_tp)(buf, L, d, q, 0)[e].ravel().tolist()
+        assert got == ints(vals), (name, q, e)
+        n += 1
+    assert n == 8
+
+
+def _silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+@pytest.mark.parametrize("w", [SMALL_W, TINY.with_(w_sigma=0.3)])
+def test_weights_tp_shards_compute_the_same_moe_ffn(w):
+    """§3: EP and TP compute the same function on the same bytes.  For every
+    expert, the EP owner's SwiGLU FFN  W2 (silu(W1 x) * (W3 x))  equals the sum
+    over TP ranks of the same FFN on their shards (the All-Reduce of §2.1)."""
+    d = dims_of(w)
+    L = oracle.layout(d)
+    buf = fill_regions(L, w, seed=11)
+    before = buf.copy()
+    oracle.weights_ep2tp(buf, d)
+    rng = np.random.default_rng(5)
+    El, Ip = d.E // d.P, d.I // d.P
+    for layer in range(d.N):
+        x = rng.normal(size=d.H)
+        for e in range(d.E):
+            r, el = divmod(e, El)
+            w13 = bf16_to_f64(w13_ep(before, L, d, r, layer + 1)[el])
+            w2 = bf16_to_f64(w2_ep(before, L, d, r, layer + 1)[el])
+            y_ep = w2 @ (_silu(w13[:d.I] @ x) * (w13[d.I:] @ x))
+            y_tp = np.zeros(d.H)
+            for q in range(d.P):
+                s13 = bf16_to_f64(w13_tp(buf, L, d, q, layer)[e])
+                s2 = bf16_to_f64(w2_tp(buf, L, d, q, layer)[e])
+                y_tp += s2 @ (_silu(s13[:Ip] @ x) * (s13[Ip:] @ x))
+            np.testing.assert_allclose(y_tp, y_ep, rtol=1e-9, atol=1e-12)
+
+
+def test_weights_contiguous_split_is_a_row_slice():
+    """w13_split = 1: TP rank q keeps W13 rows [q*2I/P, (q+1)*2I/P) (numpy slice)."""
+    w = SMALL_W
+    d = dims_of(w, w13_split=1)
+    L = oracle.layout(d)
+    buf = fill_regions(L, w, seed=3)
+    before = buf.copy()
+    oracle.weights_ep2tp(buf, d)
+    full = np.concatenate([w13_ep(before, L, d, r, 1) for r in range(d.P)])
+    rows = 2 * d.I // d.P
+    for q in range(d.P):
+        np.testing.assert_array_equal(w13_tp(buf, L, d, q, 0), full[:, q * rows:(q + 1) * rows, :])
+
+
+def test_weights_exactly_once_tagged():
+    """Every EP element lands in exactly one TP place (unique 16-bit tags)."""
+    w = TINY
+    d = dims_of(w)
+    L = oracle.layout(d)
+    El = d.E // d.P
+    n13 = d.E * 2 * d.I * d.H
+    buf = _tagged_weights(d, L, lambda e, j, h: (e * 2 * d.I + j) * d.H + h,
+                          lambda e, h, i: n13 + (e * d.H + h) * d.I + i, slot=2)
+    assert n13 + d.E * d.H * d.I <= 65536
+    oracle.weights_ep2tp(buf, d)
+    got = np.concatenate([np.concatenate([w13_tp(buf, L, d, q, 1).ravel(), w2_tp(buf, L, d, q, 1).ravel()])
+                          for q in range(d.P)])
+    assert np.array_equal(np.sort(got), np.arange(n13 + d.E * d.H * d.I))
+    # cross-region share: (P-1)/P of the moved elements change rank (§3, R-9)
+    moved_from = []
+    for q in range(d.P):
+        t13 = w13_tp(buf, L, d, q, 1).astype(np.int64)
+        e_of = t13 // (2 * d.I * d.H)
+        moved_from.append(((e_of // El) != q).sum())
+    assert sum(moved_from) == n13 * (d.P - 1) // d.P
+    del El
+
+
+def test_weights_round_trip_identity_and_untouched_bytes():
+    w = SMALL_W.with_(w_sigma=None)
+    d = dims_of(w)
+    L = oracle.layout(d)
+    buf = fill_regions(L, w, seed=7)
+    orig = buf.copy()
+    oracle.weights_ep2tp(buf, d)
+    # slot N still holds EP layer N-1 (nothing writes it, R-8)
+    for r in range(d.P):
+        a = wslot(L, r, d.N)
+        assert np.array_equal(buf[a:a + L["wslot_stride"]], orig[a:a + L["wslot_stride"]])
+    oracle.weights_tp2ep(buf, d)
+    for r in range(d.P):
+        a, b = wslot(L, r, 1), wslot(L, r, d.N + 1)
+        assert np.array_equal(buf[a:b], orig[a:b])
+    # padding between W13 and W2, and after W2, never written
+    for r in range(d.P):
+        for s in range(d.N + 1):
+            base = wslot(L, r, s)
+            w13 = (d.E // d.P) * 2 * d.I * d.H * 2
+            assert np.array_equal(buf[base + w13:base + L["w2_off"]], orig[base + w13:base + L["w2_off"]])
+
+
+def test_weights_p1_is_a_slot_shift():
+    """P = 1: both layouts coincide, so EP->TP is a plain copy slot l+1 -> slot l."""
+    w = Workload("p1", P=1, N=3, E=3, H=8, I=6)
+    d = dims_of(w)
+    L = oracle.layout(d)
+    buf = fill_regions(L, w, seed=1)
+    orig = buf.copy()
+    oracle.weights_ep2tp(buf, d)
+    s = L["wslot_stride"]
+    used = L["w2_off"] + d.E * d.H * d.I * 2
+    for layer in range(d.N):
+        np.testing.assert_array_equal(buf[layer * s + L["w13_off"]:layer * s + d.E * 2 * d.I * d.H * 2],
+                                      orig[(layer + 1) * s:(layer + 1) * s + d.E * 2 * d.I * d.H * 2])
+        np.testing.assert_array_equal(buf[layer * s + L["w2_off"]:layer * s + used],
+                                      orig[(layer + 1) * s + L["w2_off"]:(layer + 1) * s + used])
+
+
+def test_weights_w2_tp_is_a_column_slice():
+    """TP W2 of rank q = columns [q*I/P, (q+1)*I/P) of the full W2 (numpy slice)."""
+    w = SMALL_W
+    d = dims_of(w)
+    L = oracle.layout(d)
+    buf = fill_regions(L, w, seed=9)
+    before = buf.copy()
+    oracle.weights_ep2tp(buf, d)
+    Ip = d.I // d.P
+    for layer in range(d.N):
+        full = np.concatenate([w2_ep(before, L, d, r, layer + 1) for r in range(d.P)])
+        for q in range(d.P):
+            np.testing.assert_array_equal(w2_tp(buf, L, d, q, layer), full[:, :, q * Ip:(q + 1) * Ip])
+
+
+def test_layer_order_makes_in_place_safe():
+    """§4.2 Fig. 7: with the one-slot offset, EP->TP ascending and TP->EP
+    descending in place equal the copy-from-snapshot definition; the other
+    order overwrites layers before they are read."""
+    w = SMALL_W.with_(w_sigma=None)
+    d = dims_of(w)
+    L = oracle.layout(d)
+    orig = fill_regions(L, w, seed=2)
+    ref = orig.copy()
+    oracle.weights_ep2tp(ref, d, src=orig.copy())
+    ip = orig.copy()
+    oracle.weights_ep2tp(ip, d)
+    assert np.array_equal(ip, ref)
+    wrong = orig.copy()
+    oracle.weights_ep2tp(wrong, d, order=-1)
+    assert not np.array_equal(wrong, ref)
+    ref2 = ref.copy()
+    oracle.weights_tp2ep(ref2, d, src=ref.copy())
+    ip2 = ref.copy()
+    oracle.weights_tp2ep(ip2, d)
+    assert np.array_equal(ip2, ref2)
+    wrong2 = ref.copy()
+    oracle.weights_tp2ep(wrong2, d, order=1)
+    assert not np.array_equal(wrong2, ref2)
+
+
+def test_weights_byte_accounting_table1():
+    """§4.3 Table 1: the fused path writes every element once.  Written bytes
+    per layer = 2 * P * (W13 + W2 bytes of one rank); nothing else changes."""
+    w = SMALL_W.with_(w_sigma=None)
+    d = dims_of(w)
+    L = oracle.layout(d)
+    src = fill_regions(L, w, seed=4)
+    # destination pre-filled with a sentinel that the data never holds
+    src.view(np.uint16)[src.view(np.uint16) == 0xFFFF] = 0
+    dst = np.full_like(src, 0xFF)
+    oracle.weights_ep2tp(dst, d, src=src)
+    written = int((dst.view(np.uint16) != 0xFFFF).sum()) * 2
+    per_rank = (d.E // d.P) * (2 * d.I * d.H + d.H * d.I) * 2
+    assert written == d.N * d.P * per_rank
+
+
+# ----------------------------------------------------------------------------- KV
+
+def _kv_setup(w, seed=0):
+    d = dims_of(w)
+    L = oracle.layout(d)
+    st = initial_kv_state(w, d, L, seed=seed)
+    buf = fill_regions(L, w, seed=seed + 100)
+    return d, L, st, buf
+
+
+def _attention(Kt, Vt, qv):
+    s = Kt @ qv / math.sqrt(len(qv))
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    return p @ Vt
+
+
+@pytest.mark.parametrize("w", [TINY.with_(kv_sigma=1.0), SMALL_KV,
+                               SMALL_KV.with_(Hkv=8, D=4), SMALL_KV.with_(Hkv=1)])
+def test_kv_tp_heads_compute_the_same_attention(w):
+    """§3, §3.2: after EP->TP every rank holding head h computes the same
+    decode attention for every request and head as the EP owner did."""
+    d, L, st, buf = _kv_setup(w)
+    before = buf.copy()
+    assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    rng = np.random.default_rng(1)
+    for layer in range(d.N):
+        for k in range(len(st.lens)):
+            n, o = int(st.lens[k]), int(st.owner[k])
+            Ke = gather_tokens(kv_ep(before, L, d, o, layer + 1, 0), st.ep_pt[k], n)
+            Ve = gather_tokens(kv_ep(before, L, d, o, layer + 1, 1), st.ep_pt[k], n)
+            for q in range(d.P):
+                Kt = gather_tokens(kv_tp(buf, L, d, q, layer, 0), st.tp_pt[k], n)
+                Vt = gather_tokens(kv_tp(buf, L, d, q, layer, 1), st.tp_pt[k], n)
+                for hl, h in enumerate(heads_of_rank(d.P, d.Hkv, q)):
+                    qv = rng.normal(size=d.D)
+                    a_ep = _attention(bf16_to_f64(Ke[:, h]), bf16_to_f64(Ve[:, h]), qv)
+                    a_tp = _attention(bf16_to_f64(Kt[:, hl]), bf16_to_f64(Vt[:, hl]), qv)
+                    np.testing.assert_array_equal(a_tp, a_ep)
+
+
+def test_kv_golden_head_groups():
+    """§3.2 example: 4 KV heads at TP-8 -> each head on 2 ranks, and the other
+    worked cases; checked by where tagged head data lands after EP->TP."""
+    for ln in read_golden("kv_heads.txt"):
+        head, rest = ln.split(":")
+        Hkv, P = ints(head)[-2:]
+        want = [ints(x) for x in rest.split(";")]
+        w = Workload("g", P=P, N=1, Hkv=Hkv, D=2, ps=2, R=1, len_kind="uniform", len_a=3, len_b=3,
+                     slack=8.0)
+        d, L, st, buf = _kv_setup(w)
+        u = buf.view(np.uint16)
+        ep = kv_ep(buf, L, d, int(st.owner[0]), 1, 0)
+        for h in range(Hkv):
+            ep[:, :, h, :] = 1000 + h          # head tag
+        u[u == 0] = 1                           # no tag collides with filler
+        assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+        for h in range(Hkv):
+            ranks = [q for q in range(P) if (kv_tp(buf, L, d, q, 0, 0) == 1000 + h).any()]
+            assert ranks == want[h], (Hkv, P, h, ranks)
+
+
+def test_kv_exactly_once_and_replication_tagged():
+    """Every (request, token, head, dim) value appears exactly P/Hkv times
+    under TP (once when Hkv >= P), and exactly once after returning to EP."""
+    for w in (SMALL_KV.with_(kv_sigma=None), SMALL_KV.with_(Hkv=8, D=4, kv_sigma=None)):
+        d, L, st, buf = _kv_setup(w)
+        # unique tags on live EP elements (K half only; V half zero)
+        tag = 1
+        for k in range(len(st.lens)):
+            o = int(st.owner[k])
+            for c in range(2):
+                pages = kv_ep(buf, L, d, o, 1, c)
+                for t in range(int(st.lens[k])):
+                    p, s = divmod(t, d.ps)
+                    for h in range(d.Hkv):
+                        pages[st.ep_pt[k, p], s, h, :] = np.arange(tag, tag + d.D) if c == 0 else 0
+                        tag += d.D if c == 0 else 0
+        ntag = tag - 1
+        assert ntag < 65536
+        for r in range(d.P):               # clear everything else in the TP slot
+            for c in range(2):
+                kv_tp(buf, L, d, r, 0, c)[:] = 0
+        assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+        got = np.concatenate([kv_tp(buf, L, d, q, 0, 0).ravel() for q in range(d.P)])
+        cnt = np.bincount(got.astype(np.int64), minlength=ntag + 1)[1:]
+        assert (cnt == max(1, d.P // d.Hkv)).all()
+
+
+def test_kv_round_trip_is_logically_identity():
+    """EP -> TP -> EP with the greedy placement and fresh pages: every live
+    (request, token, half, head, dim) value is back, now under its new owner's
+    pages (§3.2: no request dropped, same position)."""
+    for w in (TINY, SMALL_KV.with_(kv_sigma=None)):
+        d, L, st, buf = _kv_setup(w)
+        orig = buf.copy()
+        assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+        owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+        ep_free2 = synth.permutation(9, 4, L["pages_ep"], rows=d.P)
+        fl, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, st.ep_pt.shape[1], ep_free2,
+                                         region=owner2, key=st.tp_pos)
+        assert fl == 0
+        assert oracle.kv_tp2ep(buf, d, st.lens, owner2, ep_pt2, st.tp_pt) == 0
+        for layer in range(d.N):
+            for k in range(len(st.lens)):
+                n = int(st.lens[k])
+                for c in range(2):
+                    a = gather_tokens(kv_ep(orig, L, d, int(st.owner[k]), layer + 1, c), st.ep_pt[k], n)
+                    b = gather_tokens(kv_ep(buf, L, d, int(owner2[k]), layer + 1, c), ep_pt2[k], n)
+                    np.testing.assert_array_equal(a, b)
+
+
+def test_kv_hkv_equals_p_is_a_head_transpose():
+    """Hkv = P: TP rank q's page = the EP page's head q (numpy slice)."""
+    w = SMALL_KV.with_(Hkv=4, kv_sigma=None)
+    d, L, st, buf = _kv_setup(w)
+    before = buf.copy()
+    assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    for k in range(len(st.lens)):
+        n = int(st.lens[k])
+        for p in range(n // d.ps):              # full pages only
+            src = kv_ep(before, L, d, int(st.owner[k]), 1, 0)[st.ep_pt[k, p]]
+            for q in range(d.P):
+                np.testing.assert_array_equal(kv_tp(buf, L, d, q, 0, 0)[st.tp_pt[k, p], :, 0, :],
+                                              src[:, q, :])
+
+
+def test_kv_single_request_matches_torch_index_select():
+    """One request of whole pages: the TP K cache of the head-0 rank equals
+    torch.index_select over the page-flattened EP cache."""
+    torch = pytest.importorskip("torch")
+    w = SMALL_KV.with_(R=1, len_a=12, len_b=12, kv_sigma=None, slack=4.0)   # 3 full pages of 4
+    d, L, st, buf = _kv_setup(w)
+    before = buf.copy()
+    assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    ep = torch.from_numpy(kv_ep(before, L, d, int(st.owner[0]), 1, 0).astype(np.int32))
+    tp = torch.from_numpy(kv_tp(buf, L, d, 0, 0, 0).astype(np.int32))
+    npg = 3
+    want = torch.index_select(ep, 0, torch.tensor(st.ep_pt[0, :npg], dtype=torch.long))[:, :, 0, :]
+    got = torch.index_select(tp, 0, torch.tensor(st.tp_pt[0, :npg], dtype=torch.long))[:, :, 0, :]
+    assert torch.equal(got, want)
+
+
+def test_kv_untouched_bytes_and_byte_accounting():
+    """R-8: only live token rows are written.  Bytes written per layer EP->TP =
+    tokens * max(P, Hkv) * D * 2 halves * 2 B; TP->EP = tokens * Hkv * D * 4 B."""
+    w = SMALL_KV.with_(kv_sigma=None)
+    d, L, st, src = _kv_setup(w)
+    u = src.view(np.uint16)
+    u[u == 0xFFFF] = 0
+    dst = np.full_like(src, 0xFF)
+    assert oracle.kv_ep2tp(dst, d, st.lens, st.owner, st.ep_pt, st.tp_pt, src=src) == 0
+    T = int(st.lens.sum())
+    written = int((dst.view(np.uint16) != 0xFFFF).sum()) * 2
+    assert written == d.N * T * max(d.P, d.Hkv) * d.D * 4
+    dst2 = np.full_like(src, 0xFF)
+    assert oracle.kv_tp2ep(dst2, d, st.lens, st.owner, st.ep_pt, st.tp_pt, src=src) == 0
+    written2 = int((dst2.view(np.uint16) != 0xFFFF).sum()) * 2
+    assert written2 == d.N * T * d.Hkv * d.D * 4
+
+
+def test_kv_layer_order_in_place():
+    w = SMALL_KV.with_(kv_sigma=None)
+    d, L, st, orig = _kv_setup(w)
+    ref = orig.copy()
+    oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, st.tp_pt, src=orig.copy())
+    ip = orig.copy()
+    oracle.kv_ep2tp(ip, d, st.lens, st.owner, st.ep_pt, st.tp_pt)
+    assert np.array_equal(ip, ref)
+    wrong = orig.copy()
+    oracle.kv_ep2tp(wrong, d, st.lens, st.owner, st.ep_pt, st.tp_pt, order=-1)
+    assert not np.array_equal(wrong, ref)
+
+
+def test_kv_validation_flags():
+    """§4.5 capacity check and §3.2 page tables: invalid inputs are refused
+    before anything moves (buffer unchanged)."""
+    w = SMALL_KV.with_(kv_sigma=None)
+    d, L, st, buf = _kv_setup(w)
+    orig = buf.copy()
+
+    def run(**ch):
+        a = dict(lens=st.lens.copy(), owner=st.owner.copy(), ep_pt=st.ep_pt.copy(), tp_pt=st.tp_pt.copy())
+        for key, fn in ch.items():
+            fn(a[key])
+        b = orig.copy()
+        fl = oracle.kv_ep2tp(b, d, a["lens"], a["owner"], a["ep_pt"], a["tp_pt"])
+        if fl:
+            assert np.array_equal(b, orig)
+        return fl
+
+    assert run() == 0
+    assert run(lens=lambda x: x.__setitem__(0, -1)) == oracle.F_BAD_REQUEST
+    assert run(owner=lambda x: x.__setitem__(1, d.P)) == oracle.F_BAD_REQUEST
+    assert run(ep_pt=lambda x: x.__setitem__((0, 0), L["pages_ep"])) == oracle.F_PAGE_OOB
+    assert run(tp_pt=lambda x: x.__setitem__((0, 0), -1)) == oracle.F_PAGE_OOB
+    k2 = int(np.argmax(st.lens > d.ps))
+    assert run(tp_pt=lambda x: x.__setitem__((k2, 1), x[0, 0])) == oracle.F_DUP_PAGE
+    small = dims_of(w, pages_tp=int(synth.npages(st.lens, d.ps).sum()) - 2)
+    assert oracle.kv_validate(small, 0, st.lens, st.owner, st.ep_pt, np.zeros_like(st.tp_pt)) \
+        & oracle.F_CAPACITY
+    # TP -> EP: one EP rank asked to hold more than its pool
+    many = np.zeros_like(st.owner)
+    fl = oracle.kv_validate(d, 1, st.lens, many, st.ep_pt, st.tp_pt)
+    assert fl & oracle.F_CAPACITY or fl & oracle.F_DUP_PAGE
+
+
+def test_kv_descriptors_cover_every_live_token():
+    w = SMALL_KV
+    d, L, st, _ = _kv_setup(w)
+    desc = oracle.kv_descriptors(d, 0, st.lens, st.owner, st.ep_pt, st.tp_pt)
+    assert len(desc) == int(synth.npages(st.lens, d.ps).sum())
+    assert int(desc[:, 6].sum()) == int(st.lens.sum())
+    assert (np.diff(desc[:, 2]) >= 0).all()                  # grouped by source rank
+    assert set(map(tuple, desc[:, :2].tolist())) == {(k, p) for k in range(len(st.lens))
+                                                      for p in range(int(synth.npages(st.lens[k:k + 1], d.ps)[0]))}
+
+
+# ----------------------------------------------------------------------------- requests
+
+def test_placement_golden():
+    for ln in read_golden("placement_lpt.txt"):
+        head, lens, key, owner, local, mx = ln.split("|")[0].split(":")[0], *ln.split(":", 1)[1].split("|")
+        P = ints(head.split("P=")[1])[0]
+        lens_v = ints(lens)
+        key_v = None if key.strip() == "-" else ints(key)
+        o, lp, m = oracle.place(P, lens_v, key_v)
+        assert o.tolist() == ints(owner), ln
+        assert lp.tolist() == ints(local), ln
+        assert m == ints(mx)[0], ln
+
+
+def test_placement_deterministic_and_conserving():
+    lens = synth.lengths_lognormal(0, 300, 2048, 1.0, 32768)
+    a = oracle.place(8, lens)
+    oracle.set_threads(4)
+    b = oracle.place(8, lens)
+    oracle.set_threads(1)
+    assert all(np.array_equal(x, y) for x, y in zip(a[:2], b[:2]))
+    owner, local, mx = a
+    loads = np.bincount(owner, weights=lens, minlength=8)
+    assert loads.sum() == lens.sum() and loads.max() == mx
+    for q in range(8):                        # local positions are 0..n_q-1 in list order
+        ks = np.flatnonzero(owner == q)
+        assert local[ks].tolist() == list(range(len(ks)))
+
+
+def test_placement_lpt_bound_against_brute_force():
+    """Graham's bound for longest-processing-time-first list scheduling:
+    max load <= (4/3 - 1/(3P)) * OPT, OPT found by enumerating all P^R."""
+    rng = np.random.default_rng(3)
+    for _ in range(40):
+        P = int(rng.integers(2, 4))
+        R = int(rng.integers(1, 8))
+        lens = rng.integers(1, 50, R)
+        _, _, mx = oracle.place(P, lens)
+        opt = min(max(np.bincount(np.array(a), weights=lens, minlength=P))
+                  for a in itertools.product(range(P), repeat=R))
+        assert mx <= (4 / 3 - 1 / (3 * P)) * opt + 1e-9
+        assert mx >= opt
+
+
+def test_placement_matches_heap_list_scheduling():
+    """Same result as a textbook min-heap list scheduler over the sorted list."""
+    import heapq
+    rng = np.random.default_rng(8)
+    for _ in range(30):
+        P = int(rng.integers(1, 9))
+        R = int(rng.integers(0, 60))
+        lens = rng.integers(1, 20, R)        # many ties on purpose
+        key = rng.permutation(R)
+        heap = [(0, q) for q in range(P)]
+        want = np.zeros(R, dtype=np.int64)
+        for k in sorted(range(R), key=lambda k: (-lens[k], key[k])):
+            load, q = heapq.heappop(heap)
+            want[k] = q
+            heapq.heappush(heap, (load + lens[k], q))
+        got, _, _ = oracle.place(P, lens, key)
+        assert got.tolist() == want.tolist()
+
+
+def test_request_order_golden():
+    for ln in read_golden("request_order.txt"):
+        head, rest = ln.split(":")
+        P = ints(head)[0]
+        owner, want = rest.split("|")
+        assert oracle.request_order(P, ints(owner)).tolist() == ints(want)
+
+
+def test_assign_pages_golden_and_capacity():
+    g = {ln.split(":")[0].strip(): ln.split(":")[1] for ln in read_golden("assign_pages.txt")}
+    fl, pt = oracle.assign_pages(1, ints(g["lens"]), 16, ints(g["maxp"])[0], ints(g["free"]),
+                                 key=ints(g["key"]))
+    assert fl == 0
+    assert pt.tolist() == [ints(r) for r in g["table"].split("|")]
+    fl, pt = oracle.assign_pages(1, [100, 100], 16, 8, list(range(13)))
+    assert fl == oracle.F_CAPACITY and (pt == -7).all()      # nothing written
+
+
+# ----------------------------------------------------------------------------- generator
+
+def test_generator_normal_table_and_raw():
+    t = synth.normal_table(0.02)
+    v = bf16_to_f64(t)
+    assert (np.diff(v) >= 0).all()
+    assert abs(v.mean()) < 1e-4 and abs(v.std() - 0.02) < 2e-4
+    x = synth.values_at(0, np.arange(1 << 16))
+    assert len(np.unique(x)) > 40000
+    a = synth.fill_host(1000, 5, base=123)
+    assert np.array_equal(a, synth.values_at(5, np.arange(123, 1123)))
