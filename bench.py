@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the EP<->TP reshard data plane on one GB300 (or N replicas).
+
+One step = one full switch round trip of the whole hot path on the
+full-switch workload (expert weights P=8, E=128, H=2048, I=768 over 8 layers
++ paged KV of 2048 requests, lognormal lengths with median 2048 and sigma 1.0
+capped at 32k, 4 KV heads of dim 128, page size 16, 8 layers):
+
+  EP->TP: expert weights (8 launches, ascending), request list order,
+          TP page hand-out, KV descriptors + gather/scatter (8 layers);
+  TP->EP: greedy placement, EP page hand-out, expert weights (descending),
+          KV descriptors + gather/scatter (descending).
+
+Each step starts from the EP state the previous step left (new owners, new
+pages).  The metric is reshard GB/s = algorithmic bytes read + written per
+step (one read and one write of every moved element, plus the extra writes of
+replicated KV heads) / device time.  Inputs (~260 GB) are far larger than L2,
+so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl umm|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+reshard does not shard across GPUs here); the value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth.workloads import ALL, FULL_SWITCH  # noqa: E402
+
+METRIC = "reshard GB/s (read+write) and % of HBM peak; ms per layer and per full switch"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="umm", choices=["umm", "reference"])
+    ap.add_argument("--workload", default=FULL_SWITCH.name, choices=sorted(ALL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- bytes model
+
+def algorithmic_bytes(w, lens) -> dict:
+    """Bytes the method must move (§4.3 Table 1: one read and one write per
+    moved element; EP->TP KV writes each replicated head once per replica)."""
+    out = {}
+    if w.E:
+        per_layer = 2 * w.P * (w.E // w.P) * 3 * w.I * w.H * 2      # read + write, W13 + W2
+        out["weights_per_layer"] = per_layer
+        out["weights_per_switch"] = per_layer * w.N
+    if w.Hkv:
+        T = int(np.asarray(lens, dtype=np.int64).sum())
+        rd = T * w.Hkv * w.D * 2 * 2                                # K and V, 2 B
+        wr = T * max(w.P, w.Hkv) * w.D * 2 * 2
+        out["kv_ep2tp_per_layer"] = rd + wr
+        out["kv_tp2ep_per_layer"] = 2 * rd
+        out["tokens"] = T
+    step = 2 * out.get("weights_per_switch", 0) + w.N * (out.get("kv_ep2tp_per_layer", 0) +
+                                                        out.get("kv_tp2ep_per_layer", 0))
+    out["step"] = step
+    return out
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if not self.proc or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(s):
+            m = re.match(r"([\d.]+)", s)
+            return float(m.group(1)) if m else None
+
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        mx = max((num(r[2]) or 0) for r in rows)
+        loaded = [x for x in sm if x >= 0.5 * mx] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- traffic from committed ncu summary
+
+KERNEL_SOURCES = {"kv_copy_ep2tp": "ep_tp_weight_gb300/csrc/umm_kv.cu",
+                  "weights_kernel": "ep_tp_weight_gb300/csrc/umm_weights.cu"}
+
+
+def source_digest(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this
+    workload's launch size, or None when the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
+    if not m_src or not m_tr or m_src.group(1) != source_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return int(m_tr.group(1))
+
+
+# ----------------------------------------------------------------------------- the GPU run
+
+def run_umm(args, rank, world, local_rank):
+    import torch
+    import ep_tp_weight_gb300 as umm
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = ALL[args.workload]
+    lens_h = w.lengths()
+    R = len(lens_h)
+    maxp = w.max_pages_per_req() if R else 1
+    d = w.dims()
+    dims = umm.make_dims(P=d["P"], E=d["E"], H=d["H"], I=d["I"], N=d["N"], Hkv=d["Hkv"], D=d["D"],
+                         ps=d["ps"], pages_tp=d["pages_tp"], max_requests=d["max_requests"],
+                         max_pages=d["max_pages"])
+    nbytes = umm.umm_required_bytes(dims)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)          # the one allocation (§4.2)
+    h = umm.umm_create(dims, buf, nbytes)
+    L = umm.umm_layout(h)
+    s = torch.cuda.Stream(device=dev)
+    # initial contents: every element = synth value of its index
+    tables = {}
+    mode_w, sig_w = w.w_mode()
+    plans = [(0, L["ws_off"] // 2, mode_w, sig_w)]
+    if w.Hkv:
+        mk, sk = w.kv_mode()
+        for r in range(w.P):
+            a = (r * L["region_stride"] + L["kvslots_off"]) // 2
+            plans.append((a, (w.N + 1) * L["kvslot_stride"] // 2, mk, sk))
+    for a, n, mode, sig in plans:
+        if mode and sig not in tables:
+            tables[sig] = torch.from_numpy(synth.normal_table(sig).view(np.int16).copy()).to(dev)
+        synth.fill_device(buf.data_ptr() + 2 * a, n, w.seed, mode, tables[sig].data_ptr() if mode else 0,
+                          base=a, stream=s.cuda_stream)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).to(dev)
+    have_kv = w.Hkv > 0 and R > 0
+    if have_kv:
+        P = w.P
+        lens = i32(lens_h)
+        owner = torch.empty(R, dtype=torch.int32, device=dev)
+        owner_n = torch.empty_like(owner)
+        local = torch.empty_like(owner)
+        tp_pos = torch.empty_like(owner)
+        ep_pt = torch.empty((R, maxp), dtype=torch.int32, device=dev)
+        ep_pt_n = torch.empty_like(ep_pt)
+        tp_pt = torch.empty_like(ep_pt)
+        tp_free = i32(synth.permutation(w.seed, 3, L["pages_tp"], rows=1))
+        ep_free = i32(synth.permutation(w.seed, 2, L["pages_ep"], rows=P))
+        # initial EP state: greedy owners, pages from each rank's free list
+        umm.place_requests_tp2ep(h, R, lens, None, owner, local, s)
+        umm.umm_assign_pages(h, P, R, lens, owner, None, ep_free, L["pages_ep"], L["pages_ep"], ep_pt, maxp, s)
+    torch.cuda.synchronize()
+    st = umm.umm_status_sync(h, s)
+    if st[0] != 0:
+        raise RuntimeError(f"setup failed: {umm.strerror(st[0])}")
+    state = {"owner": owner, "owner_n": owner_n, "ep_pt": ep_pt, "ep_pt_n": ep_pt_n} if have_kv else {}
+
+    ev_half = []
+
+    def step(mark=False):
+        e0 = torch.cuda.Event(enable_timing=True) if mark else None
+        if mark:
+            e0.record(s)
+        if w.E:
+            umm.reshard_weights_ep2tp(h, s)
+        if have_kv:
+            umm.gather_requests_ep2tp(h, R, state["owner"], tp_pos, s)
+            umm.umm_assign_pages(h, 1, R, lens, None, tp_pos, tp_free, L["pages_tp"], L["pages_tp"], tp_pt, maxp, s)
+            umm.reshard_kv_ep2tp(h, R, maxp, lens, state["owner"], state["ep_pt"], tp_pt, s)
+        e1 = None
+        if mark:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(s)
+        if have_kv:
+            umm.place_requests_tp2ep(h, R, lens, tp_pos, state["owner_n"], local, s)
+            umm.umm_assign_pages(h, P, R, lens, state["owner_n"], tp_pos, ep_free, L["pages_ep"], L["pages_ep"],
+                                 state["ep_pt_n"], maxp, s)
+        if w.E:
+            umm.reshard_weights_tp2ep(h, s)
+        if have_kv:
+            umm.reshard_kv_tp2ep(h, R, maxp, lens, state["owner_n"], state["ep_pt_n"], tp_pt, s)
+            state["owner"], state["owner_n"] = state["owner_n"], state["owner"]
+            state["ep_pt"], state["ep_pt_n"] = state["ep_pt_n"], state["ep_pt"]
+        if mark:
+            e2 = torch.cuda.Event(enable_timing=True)
+            e2.record(s)
+            ev_half.append((e0, e1, e2))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = umm.umm_status_sync(h, s)
+    if st[0] != 0:
+        raise RuntimeError(f"warm-up failed: {umm.strerror(st[0])}")
+    bytes_model = algorithmic_bytes(w, lens_h)
+
+    # ---------------- timed region (device time, CUDA events on the launching stream)
+    umm.umm_profile_enable(h, True)
+    umm.umm_profile_reset(h)
+    n_launch0 = umm.umm_launch_count(h)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s)
+        for _ in range(args.steps):
+            step(mark=True)
+        t1.record(s)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = t0.elapsed_time(t1)
+    launches = umm.umm_launch_count(h) - n_launch0
+    prof = {umm.KIND_NAMES[k]: umm.umm_profile_read(h, k) for k in range(umm.K_COUNT)}
+    umm.umm_profile_enable(h, False)
+    st = umm.umm_status_sync(h, s)
+    if st[0] != 0:
+        raise RuntimeError(f"timed steps failed: {umm.strerror(st[0])}")
+    ms_ep2tp = statistics.mean(a.elapsed_time(b) for a, b, _ in ev_half)
+    ms_tp2ep = statistics.mean(b.elapsed_time(c) for _, b, c in ev_half)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e and have_kv:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        h_lens = pin(lens_h.astype(np.int32))
+        h_owner = pin(state["owner"].cpu().numpy())
+        h_ep_pt = pin(state["ep_pt"].cpu().numpy())
+        h_tp_free = pin(tp_free.cpu().numpy())
+        h_ep_free = pin(ep_free.cpu().numpy())
+        o_owner = torch.empty(R, dtype=torch.int32).pin_memory()
+        o_local = torch.empty(R, dtype=torch.int32).pin_memory()
+        o_pt = torch.empty((R, maxp), dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * 4 for x in (h_lens, h_owner, h_ep_pt, h_tp_free, h_ep_free))
+        d2h = sum(x.numel() * 4 for x in (o_owner, o_local, o_pt)) + 8   # + status word read
+        barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            with torch.cuda.stream(s):
+                lens.copy_(h_lens, non_blocking=True)
+                state["owner"].copy_(h_owner, non_blocking=True)
+                state["ep_pt"].copy_(h_ep_pt, non_blocking=True)
+                tp_free.copy_(h_tp_free, non_blocking=True)
+                ep_free.copy_(h_ep_free, non_blocking=True)
+            step()
+            with torch.cuda.stream(s):
+                o_owner.copy_(state["owner"], non_blocking=True)   # the new EP owners ...
+                o_local.copy_(local, non_blocking=True)
+                o_pt.copy_(state["ep_pt"], non_blocking=True)      # ... and their pages
+            code, _ = umm.umm_status_sync(h, s)                   # syncs the stream, reads status
+            if code:
+                raise RuntimeError(f"e2e step failed: {umm.strerror(code)}")
+            h_owner.copy_(o_owner)                                 # next step starts from them
+            h_ep_pt.copy_(o_pt)
+        wall = time.perf_counter() - wall0
+        e2e_gbs = world * bytes_model["step"] * args.steps / wall / 1e9
+        e2e = {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(1e3 * wall / args.steps, 3)}
+
+    umm.umm_destroy(h)
+    del buf
+    torch.cuda.empty_cache()
+    return dict(w=w, lens=lens_h, ms_total=ms_total, launches=launches, prof=prof, clocks=clk.summary(),
+                ms_ep2tp=ms_ep2tp, ms_tp2ep=ms_tp2ep, bytes=bytes_model, e2e=e2e, layout=L, nbytes=nbytes)
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def cpu_sample(w, threads: int):
+    """The oracle timed on a bounded sample of the workload: one weight layer
+    both directions, and the first 64 requests' KV for one layer both ways."""
+    import oracle
+    oracle.set_threads(threads)
+    sample = w.with_(N=1)
+    moved = 0
+    secs = 0.0
+    if w.E:
+        ws = sample.with_(Hkv=0, R=0)
+        d = oracle.Dims(**ws.dims())
+        L = oracle.layout(d)
+        buf = np.random.default_rng(w.seed).integers(0, 256, L["ws_off"], dtype=np.uint8)
+        t = time.perf_counter()
+        oracle.weights_ep2tp(buf, d)
+        oracle.weights_tp2ep(buf, d)
+        secs += time.perf_counter() - t
+        moved += 2 * algorithmic_bytes(ws, [])["weights_per_switch"]
+        del buf
+    if w.Hkv and w.R:
+        Rs = min(64, w.R)
+        lens = w.lengths()[:Rs]
+        used = int(synth.npages(lens, w.ps).sum())
+        m = w.Hkv // w.h_tp
+        ptp = (math.ceil(1.02 * used) + m - 1) // m * m
+        kv = sample.with_(E=0, R=Rs)
+        dd = dict(kv.dims(), pages_tp=ptp, max_requests=Rs, max_pages=ptp)
+        d = oracle.Dims(**dd)
+        L = oracle.layout(d)
+        buf = np.random.default_rng(w.seed).integers(0, 256, L["ws_off"], dtype=np.uint8)
+        maxp = w.max_pages_per_req()
+        owner, _, _ = oracle.place(w.P, lens)
+        _, ep_pt = oracle.assign_pages(w.P, lens, w.ps, maxp, synth.permutation(w.seed, 2, L["pages_ep"], w.P),
+                                       region=owner)
+        pos = oracle.request_order(w.P, owner)
+        _, tp_pt = oracle.assign_pages(1, lens, w.ps, maxp, synth.permutation(w.seed, 3, L["pages_tp"]), key=pos)
+        owner2, _, _ = oracle.place(w.P, lens, key=pos)
+        _, ep_pt2 = oracle.assign_pages(w.P, lens, w.ps, maxp, synth.permutation(w.seed, 4, L["pages_ep"], w.P),
+                                        region=owner2, key=pos)
+        t = time.perf_counter()
+        assert oracle.kv_ep2tp(buf, d, lens, owner, ep_pt, tp_pt) == 0
+        assert oracle.kv_tp2ep(buf, d, lens, owner2, ep_pt2, tp_pt) == 0
+        secs += time.perf_counter() - t
+        b = algorithmic_bytes(kv.with_(R=Rs), lens)
+        moved += b["kv_ep2tp_per_layer"] + b["kv_tp2ep_per_layer"]
+    return moved, secs
+
+
+def cpu_baseline(w):
+    threads = os.cpu_count() or 1
+    moved, secs = cpu_sample(w, threads)
+    return {"value": round(moved / secs / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "plain C oracle (element by element, OpenMP): 1 expert-weight layer EP->TP->EP + "
+                      "KV of the first 64 requests for 1 layer EP->TP->EP; "
+                      f"{moved / 1e9:.2f} GB algorithmic in {secs:.2f} s"}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    w = ALL[args.workload]
+    config = {"workload": w.name, "P": w.P, "layers": w.N, "experts": w.E, "hidden": w.H,
+              "intermediate": w.I, "requests": w.R, "kv_heads": w.Hkv, "head_dim": w.D, "page_size": w.ps,
+              "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        threads = os.cpu_count() or 1
+        for _ in range(args.warmup):
+            pass   # the oracle has no warm-up state; warm-up steps would only repeat the sample
+        tot_b, tot_s = 0, 0.0
+        for _ in range(args.steps):
+            b, s = cpu_sample(w, threads)
+            tot_b += b
+            tot_s += s
+        val = tot_b / tot_s / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_s / args.steps, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(val, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                                 "sample": "each step: 1 expert-weight layer EP->TP->EP + KV of the first 64 "
+                                           "requests for 1 layer EP->TP->EP, plain C oracle"},
+                "e2e": {"value": round(val, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_umm(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    b = r["bytes"]
+    ms_step = r["ms_total"] / args.steps
+    value = world * b["step"] * args.steps / (r["ms_total"] / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    # dominant kernel = most device time in the timed region
+    prof = r["prof"]
+    dom = max(prof, key=lambda k: prof[k][1])
+    n_dom, ms_dom = prof[dom]
+    per_launch_bytes = {"kv_ep2tp": b.get("kv_ep2tp_per_layer", 0), "kv_tp2ep": b.get("kv_tp2ep_per_layer", 0),
+                        "weights_ep2tp": b.get("weights_per_layer", 0),
+                        "weights_tp2ep": b.get("weights_per_layer", 0)}.get(dom, 0)
+    achieved = per_launch_bytes / (ms_dom / n_dom / 1e3) / 1e9 if n_dom else 0.0
+    kernel_name = {"kv_ep2tp": "kv_copy_ep2tp", "weights_ep2tp": "weights_kernel"}.get(dom)
+    traffic = committed_traffic(kernel_name, r["w"].name) if kernel_name else None
+    per_kind = {k: {"launches": n, "ms_per_launch": round(ms / n, 4) if n else None}
+                for k, (n, ms) in prof.items() if n}
+    for k, key in (("weights_ep2tp", "weights_per_layer"), ("weights_tp2ep", "weights_per_layer"),
+                   ("kv_ep2tp", "kv_ep2tp_per_layer"), ("kv_tp2ep", "kv_tp2ep_per_layer")):
+        if k in per_kind and b.get(key):
+            gbs = b[key] / (per_kind[k]["ms_per_launch"] / 1e3) / 1e9
+            per_kind[k]["GB_s"] = round(gbs, 1)
+            per_kind[k]["frac_of_peak"] = round(gbs / peak, 4)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u16", "data": "synthetic (seeded; bf16 N(0,0.02) weights, N(0,1) KV)",
+        "config": config,
+        "ms_per_switch": {"ep2tp": round(r["ms_ep2tp"], 3), "tp2ep": round(r["ms_tp2ep"], 3)},
+        "ms_per_layer": {k: per_kind[k]["ms_per_launch"] for k in ("weights_ep2tp", "weights_tp2ep", "kv_ep2tp",
+                                                                   "kv_tp2ep") if k in per_kind},
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "frac_of_8TBs_nominal": round(value / world / 8000.0, 4),
+        "bytes_per_step": b["step"], "tokens": b.get("tokens"),
+        "kernels": per_kind,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} copy GB/s (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": per_launch_bytes},
+        "clocks": r["clocks"], "gpu_launches": r["launches"],
+        "e2e": r["e2e"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(r["w"])
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,250 @@
+"""Python binding of libumm (ctypes; argument marshalling only).
+
+Every function here has the name of its C entry point in include/umm.h and
+does nothing but convert arguments: torch tensors become device pointers,
+torch streams become cudaStream_t handles, non-zero status codes become
+``UmmError``.  All work runs in the library's CUDA kernels.  Importing this
+module fails loudly when libumm.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libumm.so")
+
+UMM_OK = 0
+UMM_ERR_INVALID_ARG = 1
+UMM_ERR_ALIGN = 2
+UMM_ERR_MODE = 3
+UMM_ERR_CAPACITY = 4
+UMM_ERR_PAGE_OOB = 5
+UMM_ERR_CUDA = 6
+UMM_ERR_TIMEOUT = 7
+UMM_ERR_DUP_PAGE = 8
+UMM_ERR_BAD_REQUEST = 9
+
+UMM_MODE_EP = 0
+UMM_MODE_TP = 1
+
+FLAG_BAD_REQUEST = 1
+FLAG_CAPACITY = 2
+FLAG_PAGE_OOB = 4
+FLAG_DUP_PAGE = 8
+
+K_WEIGHTS_EP2TP, K_WEIGHTS_TP2EP, K_KV_PREP, K_KV_EP2TP, K_KV_TP2EP, K_PLACE, K_ORDER, K_ASSIGN = range(8)
+K_COUNT = 8
+KIND_NAMES = ("weights_ep2tp", "weights_tp2ep", "kv_prep", "kv_ep2tp", "kv_tp2ep", "place", "order", "assign")
+
+
+class UmmDims(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int32), ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("kv_pages_tp", ctypes.c_int64), ("max_requests", ctypes.c_int32),
+                ("w13_split", ctypes.c_int32), ("max_pages", ctypes.c_int64), ("weight_mode", ctypes.c_int32),
+                ("kv_mode", ctypes.c_int32)]
+
+
+class UmmLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("region_stride", "wslot_stride", "w13_off", "w2_off",
+                                               "kvslot_stride", "kv_v_off", "kvslots_off", "ws_off",
+                                               "ws_bytes", "total_bytes")] + \
+               [(n, ctypes.c_int64) for n in ("pages_ep", "pages_tp", "h_tp")] + \
+               [("status_off", ctypes.c_uint64), ("desc_off", ctypes.c_uint64), ("desc_capacity", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class UmmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (status {code})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libumm.so is not built ({LIB_PATH}); run ep_tp_weight_gb300.build.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp, _i32, _i64, _u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+_P = ctypes.POINTER
+
+_SIG = {
+    "umm_required_bytes": [_P(UmmDims), _P(_u64)],
+    "umm_layout_for_dims": [_P(UmmDims), _P(UmmLayout)],
+    "umm_create": [_P(UmmDims), _vp, _u64, _P(_vp)],
+    "umm_destroy": [_vp],
+    "umm_layout": [_vp, _P(UmmLayout)],
+    "umm_get_modes": [_vp, _P(_i32), _P(_i32)],
+    "umm_set_modes": [_vp, _i32, _i32],
+    "reshard_weights_ep2tp": [_vp, _vp],
+    "reshard_weights_tp2ep": [_vp, _vp],
+    "gather_requests_ep2tp": [_vp, _i32, _vp, _vp, _vp],
+    "place_requests_tp2ep": [_vp, _i32, _vp, _vp, _vp, _vp, _vp],
+    "umm_assign_pages": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _i32, _vp],
+    "reshard_kv_ep2tp": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp],
+    "reshard_kv_tp2ep": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp],
+    "umm_kv_check_capacity": [_vp, _i32, _i32, _vp, _vp],
+    "umm_status_sync": [_vp, _vp, _P(_i32), _P(ctypes.c_uint32)],
+    "umm_profile_enable": [_vp, _i32],
+    "umm_profile_read": [_vp, _i32, _P(_i64), _P(ctypes.c_double)],
+    "umm_profile_reset": [_vp],
+    "umm_launch_count": [_vp, _P(_i64)],
+}
+for _name, _args in _SIG.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.umm_strerror.argtypes = [ctypes.c_int]
+_lib.umm_strerror.restype = ctypes.c_char_p
+
+EXPORTED = tuple(_SIG) + ("umm_strerror",)
+
+
+def strerror(code: int) -> str:
+    return _lib.umm_strerror(int(code)).decode()
+
+
+def _ck(rc: int, where: str) -> None:
+    if rc != UMM_OK:
+        raise UmmError(rc, where)
+
+
+def _ptr(x):
+    """Device pointer of a tensor (or an int address); None stays NULL."""
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() or None
+    return int(x) or None
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream or None
+    return int(s) or None
+
+
+def make_dims(P, E=0, H=0, I=0, N=1, Hkv=0, D=0, ps=16, pages_tp=0, max_requests=0, max_pages=0,
+              w13_split=0, weight_mode=UMM_MODE_EP, kv_mode=UMM_MODE_EP) -> UmmDims:
+    """umm_dims from the page's notation (§3.1, §3.2)."""
+    return UmmDims(P, E, H, I, N, Hkv, D, ps, pages_tp, max_requests, w13_split, max_pages,
+                   weight_mode, kv_mode)
+
+
+def umm_required_bytes(dims: UmmDims) -> int:
+    out = ctypes.c_uint64()
+    _ck(_lib.umm_required_bytes(ctypes.byref(dims), ctypes.byref(out)), "umm_required_bytes")
+    return out.value
+
+
+def umm_layout_for_dims(dims: UmmDims) -> dict:
+    out = UmmLayout()
+    _ck(_lib.umm_layout_for_dims(ctypes.byref(dims), ctypes.byref(out)), "umm_layout_for_dims")
+    return out.as_dict()
+
+
+def umm_create(dims: UmmDims, d_base, nbytes: int) -> int:
+    h = ctypes.c_void_p()
+    _ck(_lib.umm_create(ctypes.byref(dims), _ptr(d_base), int(nbytes), ctypes.byref(h)), "umm_create")
+    return h.value
+
+
+def umm_destroy(h: int) -> None:
+    _ck(_lib.umm_destroy(h), "umm_destroy")
+
+
+def umm_layout(h: int) -> dict:
+    out = UmmLayout()
+    _ck(_lib.umm_layout(h, ctypes.byref(out)), "umm_layout")
+    return out.as_dict()
+
+
+def umm_get_modes(h: int) -> tuple[int, int]:
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    _ck(_lib.umm_get_modes(h, ctypes.byref(a), ctypes.byref(b)), "umm_get_modes")
+    return a.value, b.value
+
+
+def umm_set_modes(h: int, weight_mode: int, kv_mode: int) -> None:
+    _ck(_lib.umm_set_modes(h, weight_mode, kv_mode), "umm_set_modes")
+
+
+def reshard_weights_ep2tp(h: int, stream=None) -> None:
+    _ck(_lib.reshard_weights_ep2tp(h, _stream(stream)), "reshard_weights_ep2tp")
+
+
+def reshard_weights_tp2ep(h: int, stream=None) -> None:
+    _ck(_lib.reshard_weights_tp2ep(h, _stream(stream)), "reshard_weights_tp2ep")
+
+
+def gather_requests_ep2tp(h: int, R: int, ep_owner, tp_pos, stream=None) -> None:
+    _ck(_lib.gather_requests_ep2tp(h, R, _ptr(ep_owner), _ptr(tp_pos), _stream(stream)),
+        "gather_requests_ep2tp")
+
+
+def place_requests_tp2ep(h: int, R: int, seq_lens, list_pos, owner, local_pos, stream=None) -> None:
+    _ck(_lib.place_requests_tp2ep(h, R, _ptr(seq_lens), _ptr(list_pos), _ptr(owner), _ptr(local_pos),
+                                  _stream(stream)), "place_requests_tp2ep")
+
+
+def umm_assign_pages(h: int, npools: int, R: int, seq_lens, pool, key, free_pages, free_stride: int,
+                     free_count: int, page_table, max_pages_per_req: int, stream=None) -> None:
+    _ck(_lib.umm_assign_pages(h, npools, R, _ptr(seq_lens), _ptr(pool), _ptr(key), _ptr(free_pages),
+                              int(free_stride), int(free_count), _ptr(page_table), int(max_pages_per_req),
+                              _stream(stream)), "umm_assign_pages")
+
+
+def reshard_kv_ep2tp(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner, ep_page_table,
+                     tp_page_table, stream=None) -> None:
+    _ck(_lib.reshard_kv_ep2tp(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
+                              _ptr(tp_page_table), _stream(stream)), "reshard_kv_ep2tp")
+
+
+def reshard_kv_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner, ep_page_table,
+                     tp_page_table, stream=None) -> None:
+    _ck(_lib.reshard_kv_tp2ep(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
+                              _ptr(tp_page_table), _stream(stream)), "reshard_kv_tp2ep")
+
+
+def umm_kv_check_capacity(h: int, target_kv_mode: int, R: int, h_seq_lens, h_ep_owner=None) -> int:
+    """Host-side capacity check; returns the status code (0 = fits)."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(h_seq_lens, dtype=np.int32))
+    own = None if h_ep_owner is None else np.ascontiguousarray(np.asarray(h_ep_owner, dtype=np.int32))
+    return int(_lib.umm_kv_check_capacity(h, target_kv_mode, R, lens.ctypes.data,
+                                          None if own is None else own.ctypes.data))
+
+
+def umm_status_sync(h: int, stream=None) -> tuple[int, int]:
+    """(status code, flag bits) of the device checks since the last sync; clears them."""
+    st, fl = ctypes.c_int32(), ctypes.c_uint32()
+    _ck(_lib.umm_status_sync(h, _stream(stream), ctypes.byref(st), ctypes.byref(fl)), "umm_status_sync")
+    return st.value, fl.value
+
+
+def umm_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def umm_profile_enable(h: int, enable: bool = True) -> None:
+    _ck(_lib.umm_profile_enable(h, 1 if enable else 0), "umm_profile_enable")
+
+
+def umm_profile_read(h: int, kind: int) -> tuple[int, float]:
+    n, ms = ctypes.c_int64(), ctypes.c_double()
+    _ck(_lib.umm_profile_read(h, kind, ctypes.byref(n), ctypes.byref(ms)), "umm_profile_read")
+    return n.value, ms.value
+
+
+def umm_profile_reset(h: int) -> None:
+    _ck(_lib.umm_profile_reset(h), "umm_profile_reset")
+
+
+def umm_launch_count(h: int) -> int:
+    n = ctypes.c_int64()
+    _ck(_lib.umm_launch_count(h, ctypes.byref(n)), "umm_launch_count")
+    return n.value

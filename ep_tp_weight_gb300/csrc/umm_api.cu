@@ -1,0 +1,522 @@
+// C ABI of libumm: handle, layout of the unified buffer, argument checks,
+// modes, status and per-kernel timing.  Kernels live in umm_weights.cu,
+// umm_kv.cu and umm_requests.cu.
+//
+// Layout (unified memory manager of "Moebius: Serving Mixture-of-Expert Models
+// with Seamless Runtime Parallelism Switch" (paper review), §4.2, Fig. 7): one
+// region per rank = N+1 weight slots then N+1 KV slots; TP layer l in slot l,
+// EP layer l in slot l+1; a workspace after the P regions.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "umm_internal.cuh"
+
+namespace {
+
+constexpr uint64_t kStatusBytes = 256;
+
+uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+struct Prof {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+struct KvCall {
+  unsigned int id;
+  int32_t mode_before;
+};
+
+}  // namespace
+
+struct umm {
+  umm_dims dims;
+  umm_layout_t L;
+  uk::Geo geo;
+  uk::Ws ws;
+  int device = 0;
+  int sms = 1;
+  int32_t weight_mode = UMM_MODE_EP, kv_mode = UMM_MODE_EP;
+  unsigned int next_call = 0;
+  std::vector<KvCall> kv_log;
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<Prof> pending;
+  int64_t launches = 0;   // kernels enqueued by this handle
+  int64_t prof_n[UMM_K_COUNT] = {};
+  double prof_ms[UMM_K_COUNT] = {};
+};
+
+namespace {
+
+int check_dims(const umm_dims* d) {
+  if (!d) return UMM_ERR_INVALID_ARG;
+  if (d->P < 1 || d->P > uk::kMaxGroups || d->num_layers < 1 || d->num_layers > 4096) return UMM_ERR_INVALID_ARG;
+  if (d->E < 0 || d->E % d->P) return UMM_ERR_INVALID_ARG;
+  if (d->E > 0) {
+    if (d->H < 1 || d->I < 1 || d->I % d->P) return UMM_ERR_INVALID_ARG;
+    const uint64_t el = (uint64_t)(d->E / d->P);
+    // per-region element count must stay addressable by 32-bit vector indices
+    if (el * 3ull * (uint64_t)d->I * (uint64_t)d->H >= (1ull << 31) - (1ull << 16)) return UMM_ERR_INVALID_ARG;
+  }
+  if (d->num_kv_heads < 0) return UMM_ERR_INVALID_ARG;
+  if (d->num_kv_heads > 0) {
+    const int hkv = d->num_kv_heads, P = d->P;
+    if (hkv % P != 0 && P % hkv != 0) return UMM_ERR_INVALID_ARG;
+    if (d->head_dim < 1 || d->page_size < 1 || d->kv_pages_tp < 1) return UMM_ERR_INVALID_ARG;
+    const int64_t h_tp = hkv >= P ? hkv / P : 1;
+    if (d->kv_pages_tp % (hkv / h_tp)) return UMM_ERR_INVALID_ARG;
+    if (d->kv_pages_tp >= (1ll << 31)) return UMM_ERR_INVALID_ARG;
+    if ((uint64_t)d->page_size * hkv * d->head_dim * 2 >= (1ull << 30)) return UMM_ERR_INVALID_ARG;
+  }
+  if (d->max_requests < 0 || d->max_requests > (1 << 26)) return UMM_ERR_INVALID_ARG;
+  if (d->max_pages < 0 || d->max_pages >= (1ll << 31)) return UMM_ERR_INVALID_ARG;
+  if (d->w13_split != 0 && d->w13_split != 1) return UMM_ERR_INVALID_ARG;
+  if ((d->weight_mode != UMM_MODE_EP && d->weight_mode != UMM_MODE_TP) ||
+      (d->kv_mode != UMM_MODE_EP && d->kv_mode != UMM_MODE_TP))
+    return UMM_ERR_INVALID_ARG;
+  return UMM_OK;
+}
+
+// R-1 layout: region = [weight slot 0..N][KV slot 0..N]; W2 at 256 B inside a
+// weight slot, V at 256 B after K inside a KV slot, slot strides rounded to
+// 4 KiB, region stride to 2 MiB; workspace after the last region.
+void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
+  std::memset(L, 0, sizeof(*L));
+  const uint64_t P = d->P, N = d->num_layers;
+  const uint64_t El = d->E > 0 ? (uint64_t)(d->E / d->P) : 0;
+  const uint64_t w13 = El * 2ull * d->I * d->H * 2ull;
+  const uint64_t w2 = El * (uint64_t)d->H * d->I * 2ull;
+  L->w13_off = 0;
+  L->w2_off = align_up(w13, 256);
+  L->wslot_stride = d->E > 0 ? align_up(L->w2_off + w2, 4096) : 0;
+  const int64_t hkv = d->num_kv_heads;
+  L->h_tp = hkv > 0 ? (hkv >= d->P ? hkv / d->P : 1) : 0;
+  L->pages_tp = hkv > 0 ? d->kv_pages_tp : 0;
+  L->pages_ep = hkv > 0 ? d->kv_pages_tp * L->h_tp / hkv : 0;
+  const uint64_t half = hkv > 0 ? (uint64_t)L->pages_tp * d->page_size * L->h_tp * d->head_dim * 2ull : 0;
+  L->kv_v_off = align_up(half, 256);
+  L->kvslot_stride = hkv > 0 ? align_up(L->kv_v_off + half, 4096) : 0;
+  L->kvslots_off = (N + 1) * L->wslot_stride;
+  L->region_stride = align_up((N + 1) * (L->wslot_stride + L->kvslot_stride), 2ull << 20);
+  L->ws_off = P * L->region_stride;
+
+  const int64_t desc_cap = d->max_pages > 0 ? d->max_pages : L->pages_tp;
+  const int64_t nreq = d->max_requests > 0 ? d->max_requests : 1;
+  int64_t keys_cap = 1;
+  while (keys_cap < nreq) keys_cap <<= 1;
+  const int64_t bits = std::max<int64_t>(L->pages_tp, (int64_t)P * L->pages_ep);
+  const int64_t words = (bits + 31) / 32 + 1;
+  uint64_t o = L->ws_off;
+  ws->status = o;
+  o += kStatusBytes;
+  ws->desc = o;
+  ws->desc_cap = desc_cap;
+  o = align_up(o + (uint64_t)desc_cap * sizeof(umm_kv_desc), 256);
+  ws->req_off = o;
+  o = align_up(o + (uint64_t)nreq * 8, 256);
+  ws->req_inv = o;
+  o = align_up(o + (uint64_t)nreq * 4, 256);
+  ws->keys = o;
+  ws->keys_cap = keys_cap;
+  o = align_up(o + (uint64_t)keys_cap * 8, 256);
+  ws->bitmap = o;
+  ws->bitmap_words = words;
+  o = align_up(o + (uint64_t)words * 4, 4096);
+  ws->max_requests = (int32_t)nreq;
+  L->ws_bytes = o - L->ws_off;
+  L->total_bytes = o;
+  L->status_off = ws->status;
+  L->desc_off = ws->desc;
+  L->desc_capacity = desc_cap;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+unsigned int new_call(umm* u) {
+  if (++u->next_call == 0) u->next_call = 1;
+  return u->next_call;
+}
+
+// ---- per-kernel event timing ----
+struct ProfScope {
+  umm* u;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ProfScope(umm* uu, int k, cudaStream_t ss) : u(uu), kind(k), s(ss) {
+    if (!u->prof || u->ev_pool.size() < 2) return;
+    b = u->ev_pool.back();
+    u->ev_pool.pop_back();
+    a = u->ev_pool.back();
+    u->ev_pool.pop_back();
+    cudaEventRecord(a, s);
+  }
+  ~ProfScope() {
+    if (!a) return;
+    cudaEventRecord(b, s);
+    u->pending.push_back(Prof{kind, a, b});
+  }
+};
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? UMM_OK : UMM_ERR_CUDA; }
+
+int check_kv_args(const umm* u, int32_t R, int32_t maxp, const void* a, const void* b, const void* c,
+                  const void* d) {
+  if (!u || u->dims.num_kv_heads == 0) return UMM_ERR_INVALID_ARG;
+  if (R < 0 || R > u->ws.max_requests || maxp < 1) return UMM_ERR_INVALID_ARG;
+  if ((int64_t)maxp * u->dims.page_size > 0x7fffffffll) return UMM_ERR_INVALID_ARG;
+  if (R > 0 && (!a || !b || !c || !d)) return UMM_ERR_INVALID_ARG;
+  return UMM_OK;
+}
+
+int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, const int32_t* owner,
+               const int32_t* ep_pt, const int32_t* tp_pt, void* stream) {
+  int rc = check_kv_args(u, R, maxp, lens, owner, ep_pt, tp_pt);
+  if (rc) return rc;
+  const int32_t from = dir == 0 ? UMM_MODE_EP : UMM_MODE_TP;
+  if (u->kv_mode != from) return UMM_ERR_MODE;
+  cudaStream_t s = as_stream(stream);
+  const unsigned int call = new_call(u);
+  {
+    ProfScope ps(u, UMM_K_KV_PREP, s);
+    rc = cuda_rc(uk::launch_kv_prep(u->geo, u->ws, dir, R, maxp, lens, owner, ep_pt, tp_pt, call, s, u->sms));
+  }
+  if (rc) return rc;
+  u->launches += R > 0 ? 2 : 1;
+  const int N = u->dims.num_layers;
+  for (int t = 0; t < N; ++t) {
+    const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
+    ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
+    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, s, u->sms));
+    if (rc) return rc;
+    ++u->launches;
+  }
+  u->kv_log.push_back(KvCall{call, u->kv_mode});
+  if (u->kv_log.size() > 4096) u->kv_log.erase(u->kv_log.begin());
+  u->kv_mode = dir == 0 ? UMM_MODE_TP : UMM_MODE_EP;
+  return UMM_OK;
+}
+
+int reshard_weights(umm* u, int ep2tp, void* stream) {
+  if (!u || u->dims.E == 0) return UMM_ERR_INVALID_ARG;
+  if (u->weight_mode != (ep2tp ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
+  cudaStream_t s = as_stream(stream);
+  const int N = u->dims.num_layers;
+  for (int t = 0; t < N; ++t) {
+    const int layer = ep2tp ? t : N - 1 - t;
+    ProfScope ps(u, ep2tp ? UMM_K_WEIGHTS_EP2TP : UMM_K_WEIGHTS_TP2EP, s);
+    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s, u->sms));
+    if (rc) return rc;
+    ++u->launches;
+  }
+  u->weight_mode = ep2tp ? UMM_MODE_TP : UMM_MODE_EP;
+  return UMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int umm_required_bytes(const umm_dims* dims, uint64_t* bytes_out) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!bytes_out) return UMM_ERR_INVALID_ARG;
+  umm_layout_t L;
+  uk::Ws ws;
+  compute_layout(dims, &L, &ws);
+  *bytes_out = L.total_bytes;
+  return UMM_OK;
+}
+
+int umm_layout_for_dims(const umm_dims* dims, umm_layout_t* out) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!out) return UMM_ERR_INVALID_ARG;
+  uk::Ws ws;
+  compute_layout(dims, out, &ws);
+  return UMM_OK;
+}
+
+int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!out || !d_base) return UMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_base) % 256) return UMM_ERR_ALIGN;
+  umm* u = new (std::nothrow) umm();
+  if (!u) return UMM_ERR_INVALID_ARG;
+  u->dims = *dims;
+  if (u->dims.max_pages == 0) u->dims.max_pages = dims->num_kv_heads > 0 ? dims->kv_pages_tp : 0;
+  compute_layout(&u->dims, &u->L, &u->ws);
+  if (bytes < u->L.total_bytes) {
+    delete u;
+    return UMM_ERR_CAPACITY;
+  }
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, d_base) != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    delete u;
+    return UMM_ERR_INVALID_ARG;
+  }
+  u->device = attr.device;
+  int dev_now = 0;
+  cudaGetDevice(&dev_now);
+  if (dev_now != u->device) {
+    delete u;
+    return UMM_ERR_INVALID_ARG;
+  }
+  cudaDeviceGetAttribute(&u->sms, cudaDevAttrMultiProcessorCount, u->device);
+  if (u->sms < 1) u->sms = 1;
+  uk::Geo& g = u->geo;
+  g.base = static_cast<uint8_t*>(d_base);
+  g.region_stride = u->L.region_stride;
+  g.wslot_stride = u->L.wslot_stride;
+  g.w13_off = u->L.w13_off;
+  g.w2_off = u->L.w2_off;
+  g.kvslot_stride = u->L.kvslot_stride;
+  g.kv_v_off = u->L.kv_v_off;
+  g.kvslots_off = u->L.kvslots_off;
+  g.P = dims->P;
+  g.E = dims->E;
+  g.H = dims->H;
+  g.I = dims->I;
+  g.N = dims->num_layers;
+  g.Hkv = dims->num_kv_heads;
+  g.D = dims->head_dim;
+  g.ps = dims->page_size;
+  g.w13_split = dims->w13_split;
+  g.pages_ep = u->L.pages_ep;
+  g.pages_tp = u->L.pages_tp;
+  g.h_tp = u->L.h_tp;
+  u->weight_mode = dims->weight_mode;
+  u->kv_mode = dims->kv_mode;
+  if (cudaMemset(g.base + u->ws.status, 0, kStatusBytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    delete u;
+    return UMM_ERR_CUDA;
+  }
+  *out = u;
+  return UMM_OK;
+}
+
+int umm_destroy(umm_t* u) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  for (auto& p : u->pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (auto e : u->ev_pool) cudaEventDestroy(e);
+  delete u;
+  return UMM_OK;
+}
+
+int umm_layout(const umm_t* u, umm_layout_t* out) {
+  if (!u || !out) return UMM_ERR_INVALID_ARG;
+  *out = u->L;
+  return UMM_OK;
+}
+
+int umm_get_modes(const umm_t* u, int32_t* weight_mode, int32_t* kv_mode) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  if (weight_mode) *weight_mode = u->weight_mode;
+  if (kv_mode) *kv_mode = u->kv_mode;
+  return UMM_OK;
+}
+
+int umm_set_modes(umm_t* u, int32_t weight_mode, int32_t kv_mode) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  if ((weight_mode != UMM_MODE_EP && weight_mode != UMM_MODE_TP) ||
+      (kv_mode != UMM_MODE_EP && kv_mode != UMM_MODE_TP))
+    return UMM_ERR_INVALID_ARG;
+  u->weight_mode = weight_mode;
+  u->kv_mode = kv_mode;
+  u->kv_log.clear();
+  return UMM_OK;
+}
+
+int reshard_weights_ep2tp(umm_t* u, void* stream) { return reshard_weights(u, 1, stream); }
+int reshard_weights_tp2ep(umm_t* u, void* stream) { return reshard_weights(u, 0, stream); }
+
+int gather_requests_ep2tp(umm_t* u, int32_t R, const int32_t* d_ep_owner, int32_t* d_tp_pos, void* stream) {
+  if (!u || R < 0 || R > u->ws.max_requests) return UMM_ERR_INVALID_ARG;
+  if (R > 0 && (!d_ep_owner || !d_tp_pos)) return UMM_ERR_INVALID_ARG;
+  if (R == 0) return UMM_OK;
+  cudaStream_t s = as_stream(stream);
+  const unsigned int call = new_call(u);
+  ProfScope ps(u, UMM_K_ORDER, s);
+  u->launches += 1;
+  return cuda_rc(uk::launch_order(u->geo, u->ws, R, d_ep_owner, d_tp_pos, call, s));
+}
+
+int place_requests_tp2ep(umm_t* u, int32_t R, const int32_t* d_seq_lens, const int32_t* d_list_pos,
+                         int32_t* d_owner, int32_t* d_local_pos, void* stream) {
+  if (!u || R < 0 || R > u->ws.max_requests) return UMM_ERR_INVALID_ARG;
+  if (R > 0 && (!d_seq_lens || !d_owner || !d_local_pos)) return UMM_ERR_INVALID_ARG;
+  if (R == 0) return UMM_OK;
+  cudaStream_t s = as_stream(stream);
+  const unsigned int call = new_call(u);
+  ProfScope ps(u, UMM_K_PLACE, s);
+  u->launches += 1;
+  return cuda_rc(uk::launch_place(u->geo, u->ws, R, d_seq_lens, d_list_pos, d_owner, d_local_pos, call, s));
+}
+
+int umm_assign_pages(umm_t* u, int32_t npools, int32_t R, const int32_t* d_seq_lens, const int32_t* d_pool,
+                     const int32_t* d_key, const int32_t* d_free_pages, int64_t free_stride,
+                     int64_t free_count, int32_t* d_page_table, int32_t max_pages_per_req, void* stream) {
+  if (!u || npools < 1 || npools > uk::kMaxGroups || R < 0 || R > u->ws.max_requests) return UMM_ERR_INVALID_ARG;
+  if (max_pages_per_req < 1 || free_count < 0 || (npools > 1 && free_stride < free_count))
+    return UMM_ERR_INVALID_ARG;
+  if ((int64_t)max_pages_per_req * (u->dims.page_size > 0 ? u->dims.page_size : 1) > 0x7fffffffll)
+    return UMM_ERR_INVALID_ARG;
+  if (npools > 1 && !d_pool) return UMM_ERR_INVALID_ARG;
+  if (R > 0 && (!d_seq_lens || !d_free_pages || !d_page_table)) return UMM_ERR_INVALID_ARG;
+  if (u->dims.page_size < 1) return UMM_ERR_INVALID_ARG;
+  if (R == 0) return UMM_OK;
+  cudaStream_t s = as_stream(stream);
+  const unsigned int call = new_call(u);
+  ProfScope ps(u, UMM_K_ASSIGN, s);
+  u->launches += 2;
+  return cuda_rc(uk::launch_assign(u->geo, u->ws, npools, R, d_seq_lens, d_pool, d_key, d_free_pages,
+                                   free_stride, free_count, d_page_table, max_pages_per_req, call, s, u->sms));
+}
+
+int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
+                     const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                     const int32_t* d_tp_page_table, void* stream) {
+  return reshard_kv(u, 0, R, max_pages_per_req, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table,
+                    stream);
+}
+
+int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
+                     const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                     const int32_t* d_tp_page_table, void* stream) {
+  return reshard_kv(u, 1, R, max_pages_per_req, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table,
+                    stream);
+}
+
+int umm_kv_check_capacity(const umm_t* u, int32_t target_kv_mode, int32_t R, const int32_t* h_seq_lens,
+                          const int32_t* h_ep_owner) {
+  if (!u || u->dims.num_kv_heads == 0 || R < 0 || (R > 0 && !h_seq_lens)) return UMM_ERR_INVALID_ARG;
+  if (target_kv_mode != UMM_MODE_EP && target_kv_mode != UMM_MODE_TP) return UMM_ERR_INVALID_ARG;
+  if (target_kv_mode == UMM_MODE_EP && R > 0 && !h_ep_owner) return UMM_ERR_INVALID_ARG;
+  const int64_t ps = u->dims.page_size;
+  std::vector<int64_t> per(u->dims.P, 0);
+  int64_t total = 0;
+  for (int32_t k = 0; k < R; ++k) {
+    if (h_seq_lens[k] < 0) return UMM_ERR_BAD_REQUEST;
+    const int64_t np = (h_seq_lens[k] + ps - 1) / ps;
+    total += np;
+    if (target_kv_mode == UMM_MODE_EP) {
+      const int32_t o = h_ep_owner[k];
+      if (o < 0 || o >= u->dims.P) return UMM_ERR_BAD_REQUEST;
+      per[o] += np;
+    }
+  }
+  if (total > u->L.desc_capacity) return UMM_ERR_CAPACITY;
+  if (target_kv_mode == UMM_MODE_TP) return total > u->L.pages_tp ? UMM_ERR_CAPACITY : UMM_OK;
+  for (int64_t x : per)
+    if (x > u->L.pages_ep) return UMM_ERR_CAPACITY;
+  return UMM_OK;
+}
+
+int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags_out) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  umm_status_block blk;
+  if (cudaMemcpyAsync(&blk, u->geo.base + u->ws.status, sizeof(blk), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return UMM_ERR_CUDA;
+  const uint32_t f = blk.flags;
+  int32_t code = UMM_OK;
+  if (f & UMM_FLAG_DUP_PAGE) code = UMM_ERR_DUP_PAGE;
+  if (f & UMM_FLAG_PAGE_OOB) code = UMM_ERR_PAGE_OOB;
+  if (f & UMM_FLAG_CAPACITY) code = UMM_ERR_CAPACITY;
+  if (f & UMM_FLAG_BAD_REQUEST) code = UMM_ERR_BAD_REQUEST;
+  if (f) {
+    // the first KV reshard at or after the failing call did not run, nor did
+    // any later one: the cache is still in the layout that call started from
+    for (const KvCall& c : u->kv_log)
+      if (c.id >= blk.fail_call) {
+        u->kv_mode = c.mode_before;
+        break;
+      }
+    uint32_t zero[2] = {0, 0};
+    if (cudaMemcpyAsync(u->geo.base + u->ws.status, zero, sizeof(zero), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return UMM_ERR_CUDA;
+  }
+  u->kv_log.clear();
+  if (status_out) *status_out = code;
+  if (flags_out) *flags_out = f;
+  return UMM_OK;
+}
+
+const char* umm_strerror(int code) {
+  switch (code) {
+    case UMM_OK: return "ok";
+    case UMM_ERR_INVALID_ARG: return "invalid argument";
+    case UMM_ERR_ALIGN: return "buffer base not 256-byte aligned";
+    case UMM_ERR_MODE: return "data is not in the source layout of this switch";
+    case UMM_ERR_CAPACITY: return "target capacity exceeded";
+    case UMM_ERR_PAGE_OOB: return "page id out of range";
+    case UMM_ERR_CUDA: return "CUDA runtime error";
+    case UMM_ERR_TIMEOUT: return "bounded device wait timed out";
+    case UMM_ERR_DUP_PAGE: return "destination page used twice";
+    case UMM_ERR_BAD_REQUEST: return "bad request metadata (length, owner or list position)";
+    default: return "unknown status";
+  }
+}
+
+int umm_profile_enable(umm_t* u, int32_t enable) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  u->prof = enable != 0;
+  if (u->prof && u->ev_pool.empty() && u->pending.empty()) {
+    for (int i = 0; i < 8192; ++i) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return UMM_ERR_CUDA;
+      u->ev_pool.push_back(e);
+    }
+  }
+  return UMM_OK;
+}
+
+int umm_profile_read(umm_t* u, int32_t kind, int64_t* launches, double* total_ms) {
+  if (!u || kind < 0 || kind >= UMM_K_COUNT) return UMM_ERR_INVALID_ARG;
+  for (auto& p : u->pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess)
+      return UMM_ERR_CUDA;
+    u->prof_n[p.kind] += 1;
+    u->prof_ms[p.kind] += ms;
+    u->ev_pool.push_back(p.a);
+    u->ev_pool.push_back(p.b);
+  }
+  u->pending.clear();
+  if (launches) *launches = u->prof_n[kind];
+  if (total_ms) *total_ms = u->prof_ms[kind];
+  return UMM_OK;
+}
+
+int umm_launch_count(const umm_t* u, int64_t* launches) {
+  if (!u || !launches) return UMM_ERR_INVALID_ARG;
+  *launches = u->launches;
+  return UMM_OK;
+}
+
+int umm_profile_reset(umm_t* u) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  int64_t n;
+  double ms;
+  int rc = umm_profile_read(u, 0, &n, &ms);
+  if (rc) return rc;
+  for (int k = 0; k < UMM_K_COUNT; ++k) {
+    u->prof_n[k] = 0;
+    u->prof_ms[k] = 0;
+  }
+  return UMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// Internal declarations shared by the libumm translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "umm.h"
+
+namespace uk {
+
+constexpr int kMaxGroups = 64;     // bound on P and on page-pool counts
+constexpr int kScanThreads = 1024; // threads of the single-CTA metadata kernels
+
+// Division by a runtime constant 1 <= d < 2^31 for numerators n < 2^31, by
+// multiply-high (round-up method, Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994).  With
+// s = ceil(log2 d) >= 1 and m = ceil(2^(31+s) / d) (< 2^32):
+//   n*m / 2^(31+s) = n/d + eps, 0 <= eps < n / 2^(31+s) < 2^-s <= 1/d,
+// which never carries the fraction of n/d past an integer, so
+//   floor(n/d) = umulhi(n, m) >> (s-1).   d == 1 is passed through.
+struct FastDiv {
+  uint32_t d, m, sh;
+  FastDiv() = default;
+  __host__ explicit FastDiv(uint32_t div) : d(div), m(0), sh(0) {
+    if (div <= 1) return;
+    uint32_t s = 0;
+    while ((1ull << s) < div) ++s;
+    m = (uint32_t)(((1ull << (31 + s)) + div - 1) / div);
+    sh = s - 1;
+  }
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    return d <= 1 ? n : (__umulhi(n, m) >> sh);
+#else
+    return d <= 1 ? n : (uint32_t)(((uint64_t)n * m) >> 32) >> sh;
+#endif
+  }
+  __host__ __device__ __forceinline__ void divmod(uint32_t n, uint32_t& q, uint32_t& r) const {
+    q = div(n);
+    r = n - q * d;
+  }
+};
+
+// Vector type moved per access (VB bytes); data is never interpreted.
+template <int VB> struct VecT;
+template <> struct VecT<16> { using T = uint4; };
+template <> struct VecT<8> { using T = uint2; };
+template <> struct VecT<4> { using T = uint32_t; };
+template <> struct VecT<2> { using T = unsigned short; };
+
+// Device view of the workspace status block.
+struct DevStatus {
+  unsigned int flags;
+  unsigned int fail_call;
+  unsigned long long ndesc;
+  unsigned long long tokens;
+  unsigned long long reserved[5];
+};
+static_assert(sizeof(DevStatus) == sizeof(umm_status_block), "status block layout");
+
+__device__ __forceinline__ void raise_flag(DevStatus* st, unsigned int flag, unsigned int call) {
+  atomicOr(&st->flags, flag);
+  atomicCAS(&st->fail_call, 0u, call);
+}
+
+// Everything a kernel needs to address the unified buffer.
+struct Geo {
+  uint8_t* base;
+  uint64_t region_stride, wslot_stride, w13_off, w2_off;
+  uint64_t kvslot_stride, kv_v_off, kvslots_off;
+  int32_t P, E, H, I, N, Hkv, D, ps, w13_split;
+  int64_t pages_ep, pages_tp, h_tp;
+};
+
+// Workspace carve-up (byte offsets from the buffer base).
+struct Ws {
+  uint64_t status;     // DevStatus
+  uint64_t desc;       // umm_kv_desc[desc_cap]
+  int64_t desc_cap;
+  uint64_t req_off;    // int64[max_requests]   per-request start offsets
+  uint64_t req_inv;    // int32[max_requests]   list position -> request
+  uint64_t keys;       // uint64[keys_cap]      sort keys (placement)
+  int64_t keys_cap;    // power of two >= max_requests
+  uint64_t bitmap;     // uint32[bitmap_words]  destination-page use bits
+  int64_t bitmap_words;
+  int32_t max_requests;
+};
+
+// ---- launchers (enqueue only; all arguments already validated) ----
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, int sms);
+
+cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_t maxp,
+                           const int32_t* lens, const int32_t* owner, const int32_t* ep_pt,
+                           const int32_t* tp_pt, unsigned int call, cudaStream_t s, int sms);
+cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, cudaStream_t s, int sms);
+
+cudaError_t launch_order(const Geo& g, const Ws& w, int32_t R, const int32_t* owner, int32_t* tp_pos,
+                         unsigned int call, cudaStream_t s);
+cudaError_t launch_place(const Geo& g, const Ws& w, int32_t R, const int32_t* lens,
+                         const int32_t* list_pos, int32_t* owner, int32_t* local_pos,
+                         unsigned int call, cudaStream_t s);
+cudaError_t launch_assign(const Geo& g, const Ws& w, int32_t npools, int32_t R, const int32_t* lens,
+                          const int32_t* pool, const int32_t* key, const int32_t* free_pages,
+                          int64_t free_stride, int64_t free_count, int32_t* pt, int32_t maxp,
+                          unsigned int call, cudaStream_t s, int sms);
+
+}  // namespace uk

@@ -1,0 +1,273 @@
+// Request metadata of a switch: the EP->TP global list order, the TP->EP
+// greedy placement, and destination page hand-out.
+//
+// "Moebius: Serving Mixture-of-Expert Models with Seamless Runtime Parallelism
+// Switch" (paper review), §3.2: on EP->TP a metadata all-gather gives every
+// rank the same ordered in-flight list; on TP->EP the list is sorted by
+// sequence length (longest first) and each request goes to the least-loaded
+// rank -- deterministic, so every rank computes the same partition without
+// communicating.  Requests then move to "reassigned target pages".
+//
+// These kernels are tiny next to the data movement; each runs as one CTA
+// (plus a wide fill for page tables), with ballot-free block scans.
+#include <climits>
+
+#include "umm_scan.cuh"
+
+namespace uk {
+
+// ------------------------------------------------------------------ list order (EP -> TP)
+
+__global__ void __launch_bounds__(kScanThreads)
+order_kernel(Geo g, Ws w, int32_t R, const int32_t* __restrict__ owner, int32_t* __restrict__ tp_pos,
+             unsigned int call) {
+  DevStatus* st = status_of(g, w);
+  if (read_flags(st)) return;
+  __shared__ long long carry[kMaxGroups];
+  __shared__ long long warp_tot[32 * kMaxGroups];
+  __shared__ unsigned long long cnt[kMaxGroups];
+  __shared__ int bad;
+  const int tid = threadIdx.x, P = g.P;
+  if (tid < kMaxGroups) cnt[tid] = 0;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  for (int k = tid; k < R; k += blockDim.x) {
+    const int o = owner[k];
+    if (o < 0 || o >= P) bad = 1;
+    else atomicAdd(&cnt[o], 1ull);
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) raise_flag(st, UMM_FLAG_BAD_REQUEST, call);
+    return;
+  }
+  if (tid == 0) {
+    long long run = 0;
+    for (int r = 0; r < P; ++r) {
+      carry[r] = run;     // rank r's requests follow those of ranks < r
+      run += (long long)cnt[r];
+    }
+  }
+  __syncthreads();
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int k = base + tid;
+    const long long pre = group_exclusive_scan(k < R ? 1 : 0, k < R ? owner[k] : 0, P, carry, warp_tot);
+    if (k < R) tp_pos[k] = (int32_t)pre;
+  }
+}
+
+cudaError_t launch_order(const Geo& g, const Ws& w, int32_t R, const int32_t* owner, int32_t* tp_pos,
+                         unsigned int call, cudaStream_t s) {
+  order_kernel<<<1, kScanThreads, 0, s>>>(g, w, R, owner, tp_pos, call);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ shared checks
+
+// inv[pos] = k for the list positions pos = key[k]; returns false unless the
+// keys are a permutation of 0..R-1.  Block-wide; all threads return the same.
+static __device__ bool build_inverse(const int32_t* __restrict__ key, int32_t R, int32_t* inv, int* bad_flag) {
+  for (int k = threadIdx.x; k < R; k += blockDim.x) {
+    const int pos = key[k];
+    if (pos < 0 || pos >= R) *bad_flag = 1;
+    else inv[pos] = k;
+  }
+  __syncthreads();
+  if (!*bad_flag)
+    for (int k = threadIdx.x; k < R; k += blockDim.x)
+      if (inv[key[k]] != k) *bad_flag = 1;   // a repeated position left another k there
+  __syncthreads();
+  return *bad_flag == 0;
+}
+
+// ------------------------------------------------------------------ placement (TP -> EP)
+
+// Greedy list scheduling with the loads held in registers (PB >= P).
+template <int PB>
+__device__ void greedy(const unsigned long long* keys, int32_t R, int P, const int32_t* inv,
+                       int32_t* owner) {
+  long long load[PB];
+#pragma unroll
+  for (int q = 0; q < PB; ++q) load[q] = q < P ? 0 : LLONG_MAX;
+  for (int i = 0; i < R; ++i) {
+    const unsigned long long key = keys[i];
+    const int pos = (int)(key & 0xffffffffu);
+    const long long len = 0x7fffffffll - (long long)(key >> 32);
+    int best = 0;
+    long long bl = load[0];
+#pragma unroll
+    for (int q = 1; q < PB; ++q)
+      if (load[q] < bl) { bl = load[q]; best = q; }   // strict: ties keep the lower rank
+#pragma unroll
+    for (int q = 0; q < PB; ++q)
+      if (q == best) load[q] += len;
+    owner[inv ? inv[pos] : pos] = best;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+place_kernel(Geo g, Ws w, int32_t R, const int32_t* __restrict__ lens, const int32_t* __restrict__ list_pos,
+             int32_t* __restrict__ owner, int32_t* __restrict__ local_pos, int keys_in_smem,
+             unsigned int call) {
+  DevStatus* st = status_of(g, w);
+  if (read_flags(st)) return;
+  extern __shared__ unsigned long long smem_keys[];
+  __shared__ long long carry[kMaxGroups];
+  __shared__ long long warp_tot[32 * kMaxGroups];
+  __shared__ int bad;
+  const int tid = threadIdx.x, P = g.P;
+  if (tid == 0) bad = 0;
+  if (tid < kMaxGroups) carry[tid] = 0;
+  __syncthreads();
+  for (int k = tid; k < R; k += blockDim.x)
+    if (lens[k] < 0) bad = 1;
+  __syncthreads();
+  int32_t* inv = reinterpret_cast<int32_t*>(g.base + w.req_inv);
+  bool ok = bad == 0;
+  if (ok && list_pos) ok = build_inverse(list_pos, R, inv, &bad);
+  if (!ok) {
+    if (tid == 0) raise_flag(st, UMM_FLAG_BAD_REQUEST, call);
+    return;
+  }
+  // keys: (length descending, list position ascending), unique
+  int n2 = 1;
+  while (n2 < R) n2 <<= 1;
+  unsigned long long* keys =
+      keys_in_smem ? smem_keys : reinterpret_cast<unsigned long long*>(g.base + w.keys);
+  for (int i = tid; i < n2; i += blockDim.x) {
+    unsigned long long kk = ~0ull;
+    if (i < R) {
+      const unsigned long long pos = list_pos ? (unsigned long long)list_pos[i] : (unsigned long long)i;
+      kk = ((unsigned long long)(0x7fffffffll - lens[i]) << 32) | pos;
+    }
+    keys[i] = kk;
+  }
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n2; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const unsigned long long a = keys[i], b = keys[j];
+          if ((a > b) == up) { keys[i] = b; keys[j] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    const int32_t* iv = list_pos ? inv : nullptr;
+    if (P <= 8) greedy<8>(keys, R, P, iv, owner);
+    else if (P <= 16) greedy<16>(keys, R, P, iv, owner);
+    else if (P <= 32) greedy<32>(keys, R, P, iv, owner);
+    else greedy<64>(keys, R, P, iv, owner);
+  }
+  __syncthreads();
+  // local position = rank among the owner's requests in list order
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int pos = base + tid;
+    int k = 0, grp = 0;
+    if (pos < R) {
+      k = list_pos ? inv[pos] : pos;
+      grp = owner[k];
+    }
+    const long long pre = group_exclusive_scan(pos < R ? 1 : 0, grp, P, carry, warp_tot);
+    if (pos < R) local_pos[k] = (int32_t)pre;
+  }
+}
+
+cudaError_t launch_place(const Geo& g, const Ws& w, int32_t R, const int32_t* lens, const int32_t* list_pos,
+                         int32_t* owner, int32_t* local_pos, unsigned int call, cudaStream_t s) {
+  int n2 = 1;
+  while (n2 < R) n2 <<= 1;
+  const size_t need = (size_t)n2 * sizeof(unsigned long long);
+  const int in_smem = need <= 128 * 1024;
+  const size_t dyn = in_smem ? need : 0;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  place_kernel<<<1, kScanThreads, dyn, s>>>(g, w, R, lens, list_pos, owner, local_pos, in_smem, call);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ page hand-out
+
+__global__ void __launch_bounds__(kScanThreads)
+assign_scan(Geo g, Ws w, int32_t npools, int32_t R, int32_t maxp, const int32_t* __restrict__ lens,
+            const int32_t* __restrict__ pool, const int32_t* __restrict__ key, int64_t free_count,
+            unsigned int call) {
+  DevStatus* st = status_of(g, w);
+  if (read_flags(st)) return;
+  __shared__ long long carry[kMaxGroups];
+  __shared__ long long warp_tot[32 * kMaxGroups];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) bad = 0;
+  if (tid < kMaxGroups) carry[tid] = 0;
+  __syncthreads();
+  const long long max_len = (long long)maxp * g.ps;
+  for (int k = tid; k < R; k += blockDim.x) {
+    const int len = lens[k];
+    const int pl = pool ? pool[k] : 0;
+    if (len < 0 || (long long)len > max_len || pl < 0 || pl >= npools) bad = 1;
+  }
+  __syncthreads();
+  int32_t* inv = reinterpret_cast<int32_t*>(g.base + w.req_inv);
+  bool ok = bad == 0;
+  if (ok && key) ok = build_inverse(key, R, inv, &bad);
+  if (!ok) {
+    if (tid == 0) raise_flag(st, UMM_FLAG_BAD_REQUEST, call);
+    return;
+  }
+  int64_t* start = reinterpret_cast<int64_t*>(g.base + w.req_off);
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int pos = base + tid;
+    int k = 0, grp = 0;
+    long long np = 0;
+    if (pos < R) {
+      k = key ? inv[pos] : pos;
+      grp = pool ? pool[k] : 0;
+      np = (lens[k] + g.ps - 1) / g.ps;
+    }
+    const long long pre = group_exclusive_scan(np, grp, npools, carry, warp_tot);
+    if (pos < R) start[k] = pre;
+  }
+  if (tid < npools && carry[tid] > free_count) raise_flag(st, UMM_FLAG_CAPACITY, call);
+}
+
+__global__ void __launch_bounds__(256)
+assign_emit(Geo g, Ws w, int32_t R, int32_t maxp, const int32_t* __restrict__ lens,
+            const int32_t* __restrict__ pool, const int32_t* __restrict__ free_pages, int64_t free_stride,
+            int32_t* __restrict__ pt) {
+  const DevStatus* st = status_of(g, w);
+  if (read_flags(st)) return;
+  const int lane = threadIdx.x & 31;
+  const int warps_total = (gridDim.x * blockDim.x) >> 5;
+  const int64_t* start = reinterpret_cast<const int64_t*>(g.base + w.req_off);
+  for (int k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < R; k += warps_total) {
+    const int np = (lens[k] + g.ps - 1) / g.ps;
+    const int64_t src = (pool ? (int64_t)pool[k] : 0) * free_stride + start[k];
+    int32_t* row = pt + (int64_t)k * maxp;
+    for (int p = lane; p < maxp; p += 32) row[p] = p < np ? free_pages[src + p] : -1;
+  }
+}
+
+cudaError_t launch_assign(const Geo& g, const Ws& w, int32_t npools, int32_t R, const int32_t* lens,
+                          const int32_t* pool, const int32_t* key, const int32_t* free_pages,
+                          int64_t free_stride, int64_t free_count, int32_t* pt, int32_t maxp,
+                          unsigned int call, cudaStream_t s, int sms) {
+  assign_scan<<<1, kScanThreads, 0, s>>>(g, w, npools, R, maxp, lens, pool, key, free_count, call);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || R == 0) return e;
+  int blocks = (R * 32 + 255) / 256;
+  if (blocks > sms * 8) blocks = sms * 8;
+  assign_emit<<<blocks, 256, 0, s>>>(g, w, R, maxp, lens, pool, free_pages, free_stride, pt);
+  return cudaGetLastError();
+}
+
+}  // namespace uk

@@ -1,0 +1,167 @@
+// Expert-weight reshard EP <-> TP, one layer per launch.
+//
+// "Moebius: Serving Mixture-of-Expert Models with Seamless Runtime Parallelism
+// Switch" (paper review): §3.1 (layouts and the permute -> exchange -> scatter
+// pipeline), §4.2 Fig. 7 (N+1 slots, in-place layer order), §4.3 Table 1 and
+// Fig. 8a (fused direct transfer: one read + one write per element, no staging).
+//
+// On one GPU the P ranks are P regions of one buffer, so the three stages
+// collapse into a single pass: every thread reads 16-byte vectors of the EP
+// view and writes them straight to their TP place (EP->TP) or the other way
+// round (TP->EP).  Work is walked in EP order, where both W13 and W2 of a
+// region are contiguous: the EP side is streamed linearly, the TP side is P
+// sequential streams (W13: whole rows of H elements; W2: runs of I/P
+// elements), so every DRAM sector moved is fully used.
+#include "umm_internal.cuh"
+
+namespace uk {
+
+struct WParams {
+  uint8_t* base;
+  uint64_t region_stride, w13_off, w2_off;
+  uint64_t ep_slot_off, tp_slot_off;  // slot offsets inside a region
+  uint64_t w13_row_bytes;             // H * 2
+  uint64_t w2_tp_row_bytes;           // Ip * 2
+  uint32_t El, Ip, H;
+  uint32_t v13, vr;                   // W13 vectors per region, W13+W2 vectors per region
+  uint32_t tiles_total;
+  FastDiv hv, two_i, i_d, ip_d, two_ip, iv, ipv, tiles_per_region;
+  int split;
+};
+
+template <int VB, int U, int T>
+__global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) {
+  using V = typename VecT<VB>::T;
+  for (uint32_t tile = blockIdx.x; tile < p.tiles_total; tile += gridDim.x) {
+    uint32_t r, lt;
+    p.tiles_per_region.divmod(tile, r, lt);
+    uint8_t* const region_r = p.base + (uint64_t)r * p.region_stride;
+    const uint32_t v0 = lt * (uint32_t)(T * U) + threadIdx.x;
+
+    V val[U];
+    uint8_t* tp_addr[U];
+    uint8_t* ep_addr[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = v0 + (uint32_t)(u * T);
+      ep_addr[u] = nullptr;
+      if (v < p.vr) {
+        ep_addr[u] = region_r + p.ep_slot_off +
+                     (v < p.v13 ? p.w13_off + (uint64_t)v * VB : p.w2_off + (uint64_t)(v - p.v13) * VB);
+      }
+    }
+    // The TP address of each vector.  EP W13 row (e_l, j) of region r holds
+    // expert e = r*El + e_l; with j = g*I + i (g: gate/up), it is TP rank
+    // i / Ip's row g*Ip + i % Ip (split 0) or rank j / 2Ip's row j % 2Ip
+    // (split 1).  EP W2 row (e_l, h), column i belongs to TP rank i / Ip,
+    // row r*El*H + e_l*H + h, column i % Ip.
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = v0 + (uint32_t)(u * T);
+      tp_addr[u] = nullptr;
+      if (v >= p.vr) continue;
+      if (v < p.v13) {
+        uint32_t row_all, hv, el, j, q, trow;
+        p.hv.divmod(v, row_all, hv);
+        p.two_i.divmod(row_all, el, j);
+        if (p.split == 0) {
+          uint32_t g, i, ii;
+          p.i_d.divmod(j, g, i);
+          p.ip_d.divmod(i, q, ii);
+          trow = g * p.Ip + ii;
+        } else {
+          p.two_ip.divmod(j, q, trow);
+        }
+        const uint64_t e = (uint64_t)r * p.El + el;
+        tp_addr[u] = p.base + (uint64_t)q * p.region_stride + p.tp_slot_off + p.w13_off +
+                     (e * 2 * p.Ip + trow) * p.w13_row_bytes + (uint64_t)hv * VB;
+      } else {
+        uint32_t row_all, iv, q, cc;
+        p.iv.divmod(v - p.v13, row_all, iv);
+        p.ipv.divmod(iv, q, cc);
+        const uint64_t trow = (uint64_t)r * p.El * p.H + row_all;
+        tp_addr[u] = p.base + (uint64_t)q * p.region_stride + p.tp_slot_off + p.w2_off +
+                     trow * p.w2_tp_row_bytes + (uint64_t)cc * VB;
+      }
+    }
+    if (ep2tp) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ep_addr[u]) val[u] = __ldcs(reinterpret_cast<const V*>(ep_addr[u]));
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ep_addr[u]) __stcs(reinterpret_cast<V*>(tp_addr[u]), val[u]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ep_addr[u]) val[u] = __ldcs(reinterpret_cast<const V*>(tp_addr[u]));
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ep_addr[u]) __stcs(reinterpret_cast<V*>(ep_addr[u]), val[u]);
+    }
+  }
+}
+
+namespace {
+constexpr int kT = 256;
+constexpr int kU = 8;
+
+template <int VB>
+cudaError_t run(const WParams& p, int ep2tp, cudaStream_t s, int sms) {
+  static int occ = 0;
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, weights_kernel<VB, kU, kT>, kT, 0);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+  }
+  uint32_t grid = (uint32_t)sms * (uint32_t)occ;
+  if (grid > p.tiles_total) grid = p.tiles_total;
+  if (grid == 0) return cudaSuccess;
+  weights_kernel<VB, kU, kT><<<grid, kT, 0, s>>>(p, ep2tp);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, int sms) {
+  const uint32_t El = (uint32_t)(g.E / g.P), Ip = (uint32_t)(g.I / g.P), H = (uint32_t)g.H;
+  const uint32_t I = (uint32_t)g.I;
+  int VB = 2;
+  if (H % 8 == 0 && Ip % 8 == 0) VB = 16;
+  else if (H % 4 == 0 && Ip % 4 == 0) VB = 8;
+  else if (H % 2 == 0 && Ip % 2 == 0) VB = 4;
+  const uint32_t per = (uint32_t)VB / 2;  // elements per vector
+  WParams p;
+  p.base = g.base;
+  p.region_stride = g.region_stride;
+  p.w13_off = g.w13_off;
+  p.w2_off = g.w2_off;
+  p.ep_slot_off = (uint64_t)(layer + 1) * g.wslot_stride;
+  p.tp_slot_off = (uint64_t)layer * g.wslot_stride;
+  p.w13_row_bytes = (uint64_t)H * 2;
+  p.w2_tp_row_bytes = (uint64_t)Ip * 2;
+  p.El = El;
+  p.Ip = Ip;
+  p.H = H;
+  p.v13 = (uint32_t)((uint64_t)El * 2 * I * H / per);
+  p.vr = p.v13 + (uint32_t)((uint64_t)El * H * I / per);
+  const uint32_t tile = (uint32_t)(kT * kU);
+  const uint32_t tpr = (p.vr + tile - 1) / tile;
+  p.tiles_total = tpr * (uint32_t)g.P;
+  p.hv = FastDiv(H / per);
+  p.two_i = FastDiv(2 * I);
+  p.i_d = FastDiv(I);
+  p.ip_d = FastDiv(Ip);
+  p.two_ip = FastDiv(2 * Ip);
+  p.iv = FastDiv(I / per);
+  p.ipv = FastDiv(Ip / per);
+  p.tiles_per_region = FastDiv(tpr);
+  p.split = g.w13_split;
+  switch (VB) {
+    case 16: return run<16>(p, ep2tp, s, sms);
+    case 8: return run<8>(p, ep2tp, s, sms);
+    case 4: return run<4>(p, ep2tp, s, sms);
+    default: return run<2>(p, ep2tp, s, sms);
+  }
+}
+
+}  // namespace uk

@@ -1,0 +1,275 @@
+/*
+ * umm.h -- C ABI of libumm: the data plane of a runtime EP <-> TP parallelism
+ * switch for Mixture-of-Experts serving, on one GPU.
+ *
+ * Method: "Moebius: Serving Mixture-of-Expert Models with Seamless Runtime
+ * Parallelism Switch" (paper review page).  Sections cited below are that
+ * paper's:
+ *   §3    EP and TP are two layouts of the same bytes; a switch only moves the
+ *         bytes whose owner changes.
+ *   §3.1  Weight layouts.  EP: rank r owns experts [r*E/P, (r+1)*E/P) whole,
+ *         W13 (E/P, 2I, H), W2 (E/P, H, I).  TP: every rank owns a 1/P shard of
+ *         every expert, W13 (E, 2I/P, H), W2 (E, H, I/P).
+ *   §3.2  KV cache: EP ranks keep all KV heads of their own requests; TP ranks
+ *         keep a head shard of every request, heads replicated over rank
+ *         groups when KV heads < P.  EP->TP request order comes from a metadata
+ *         all-gather; TP->EP placement is greedy (longest first, least-loaded
+ *         rank), deterministic.  Paged KV is moved through the page tables.
+ *   §4.2, Fig. 7  Unified memory manager: one fixed buffer, N+1 per-layer
+ *         slots, TP layer i in slot i and EP layer i in slot i+1; EP->TP walks
+ *         layers ascending, TP->EP descending, so the reshard is in place, with
+ *         no allocation and fixed tensor addresses (captured graphs stay valid).
+ *   §4.3, Table 1, Fig. 8  Fused direct-transfer kernels: one read and one
+ *         write per moved element, no staging, page-indexed work descriptors
+ *         for the KV cache.
+ *   §4.5  Before committing, check that the target layout's KV capacity holds
+ *         the live requests.
+ *
+ * Here the P ranks are P fixed regions of ONE device buffer on one GPU, so
+ * every "exchange" is an on-device copy.
+ *
+ * Conventions for every entry point:
+ *  - Return value: UMM_OK (0) or a UMM_ERR_* code.  Host-detectable errors
+ *    (bad sizes, null pointers, misalignment, wrong mode) are returned
+ *    synchronously and nothing is enqueued.
+ *  - Device pointers ("d_" prefix) must point to device memory of the GPU the
+ *    buffer lives on; host pointers have the "h_" prefix.  All int32 arrays
+ *    are caller-owned; the library never allocates, frees or keeps them.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls enqueue
+ *    kernels on it and return without synchronising; they call no cudaMalloc
+ *    and never move the buffer.  Calls on one handle must be issued to one
+ *    stream at a time (they share the workspace).
+ *  - Device-detected errors (page table contents, capacity, bad lengths) are
+ *    found before any byte of the buffer is written.  They set sticky flags in
+ *    the workspace; every later validating kernel (KV, placement, request
+ *    order, page hand-out) then does nothing until umm_status_sync() reads and
+ *    clears them.  Weight reshards cannot fail on the device and ignore them.
+ *  - The library never aborts, traps or throws across this ABI.
+ */
+#ifndef UMM_H_
+#define UMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define UMM_OK               0
+#define UMM_ERR_INVALID_ARG  1  /* bad sizes, null pointer, R > max_requests, ...        */
+#define UMM_ERR_ALIGN        2  /* buffer base not 256-byte aligned                       */
+#define UMM_ERR_MODE         3  /* e.g. EP->TP requested while the data is already TP     */
+#define UMM_ERR_CAPACITY     4  /* target pool / descriptor space too small (§4.5)         */
+#define UMM_ERR_PAGE_OOB     5  /* a page id outside its pool                             */
+#define UMM_ERR_CUDA         6  /* a CUDA runtime call failed                             */
+#define UMM_ERR_TIMEOUT      7  /* reserved: a bounded device wait gave up                */
+#define UMM_ERR_DUP_PAGE     8  /* two live pages would be written to one destination page */
+#define UMM_ERR_BAD_REQUEST  9  /* length < 0 or > max_pages_per_req*page_size, owner or
+                                   list position out of range                             */
+
+#define UMM_MODE_EP 0
+#define UMM_MODE_TP 1
+
+/* ---- sizes (§3.1, §3.2) ----
+ * P ranks, E experts, H hidden size, I expert intermediate size, num_layers N.
+ * Requirements: P >= 1, E % P == 0, I % P == 0, N >= 1.  E == 0 means "no
+ * expert weights".  num_kv_heads == 0 means "no KV cache"; otherwise
+ * num_kv_heads % P == 0 or P % num_kv_heads == 0, head_dim >= 1,
+ * page_size >= 1 and kv_pages_tp a multiple of num_kv_heads / h_tp, where
+ * h_tp = max(1, num_kv_heads / P) is the number of heads a TP rank keeps.
+ * Elements are 2 bytes (bf16) and are moved as opaque bit patterns. */
+typedef struct {
+  int32_t P, E, H, I, num_layers;
+  int32_t num_kv_heads, head_dim, page_size;
+  int64_t kv_pages_tp;     /* TP-view pages per region and KV slot (K and V each)   */
+  int32_t max_requests;    /* largest R any request call may pass                   */
+  int32_t w13_split;       /* 0: TP rank q keeps gate rows [q*I/P,(q+1)*I/P) then the
+                              same rows of up (SwiGLU stays rank-local); 1: rows
+                              [q*2I/P, (q+1)*2I/P) of W13                             */
+  int64_t max_pages;       /* descriptor capacity: most live pages in one KV call
+                              (0 = kv_pages_tp)                                      */
+  int32_t weight_mode;     /* layout the weights are in at create (UMM_MODE_*)      */
+  int32_t kv_mode;         /* layout the KV cache is in at create                   */
+} umm_dims;
+
+/* ---- buffer layout (all offsets in bytes from the buffer base) ----
+ * region r (rank r) starts at r * region_stride and holds
+ *   weight slot s (s = 0..N) at  r*region_stride + s*wslot_stride:
+ *       W13 at +w13_off, W2 at +w2_off;
+ *       EP view of layer l = slot l+1: W13 [E/P][2I][H], W2 [E/P][H][I]
+ *       TP view of layer l = slot l:   W13 [E][2I/P][H], W2 [E][H][I/P]
+ *   KV slot s (s = 0..N) at     r*region_stride + kvslots_off + s*kvslot_stride:
+ *       K half at +0, V half at +kv_v_off; each half is a page pool
+ *       EP view of layer l = slot l+1: [pages_ep][page_size][num_kv_heads][head_dim]
+ *       TP view of layer l = slot l:   [pages_tp][page_size][h_tp][head_dim]
+ * The workspace (status, descriptors, scratch) follows the P regions at
+ * ws_off; callers must not write it.  total_bytes = ws_off + ws_bytes. */
+typedef struct {
+  uint64_t region_stride, wslot_stride, w13_off, w2_off;
+  uint64_t kvslot_stride, kv_v_off, kvslots_off;
+  uint64_t ws_off, ws_bytes, total_bytes;
+  int64_t pages_ep, pages_tp, h_tp;
+  uint64_t status_off;     /* umm_status_block                                      */
+  uint64_t desc_off;       /* umm_kv_desc[desc_capacity]                             */
+  int64_t desc_capacity;
+} umm_layout_t;
+
+/* Workspace status block (device memory, at status_off). */
+typedef struct {
+  uint32_t flags;          /* sticky UMM_FLAG_* bits                                 */
+  uint32_t fail_call;      /* id of the first call that raised a flag (0 = none)     */
+  uint64_t ndesc;          /* descriptors written by the last KV call                */
+  uint64_t tokens;         /* live tokens of the last KV call                        */
+  uint64_t reserved[5];
+} umm_status_block;
+
+#define UMM_FLAG_BAD_REQUEST 1u
+#define UMM_FLAG_CAPACITY    2u
+#define UMM_FLAG_PAGE_OOB    4u
+#define UMM_FLAG_DUP_PAGE    8u
+
+/* One page-indexed work descriptor (§4.3): the live tokens of logical page
+ * `page` of request `req`.  Descriptors are grouped by the rank whose bytes
+ * they move (EP->TP: the EP owner read from; TP->EP: the EP owner written
+ * to), then by request, then by page.  src_region / dst_region = -1 means
+ * "per head: the TP rank(s) holding it". */
+typedef struct {
+  int32_t req, page, src_region, dst_region, src_page, dst_page, ntok, reserved;
+} umm_kv_desc;
+
+typedef struct umm umm_t;  /* opaque host handle, owned by the library */
+
+/* Bytes the caller must allocate for `dims` (host-only computation). */
+int umm_required_bytes(const umm_dims* dims, uint64_t* bytes_out);
+
+/* Layout for `dims` without a handle (host-only computation). */
+int umm_layout_for_dims(const umm_dims* dims, umm_layout_t* out);
+
+/* Bind a handle to a caller-owned device buffer of at least
+ * umm_required_bytes() bytes, base 256-byte aligned (§4.2: the one
+ * allocation, made once at start-up).  Initialises the workspace status block
+ * (synchronous memset); everything else in the buffer is left as is.
+ * Errors: INVALID_ARG, ALIGN, CAPACITY (bytes too small), CUDA. */
+int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out);
+
+/* Release the host handle.  The buffer stays the caller's. */
+int umm_destroy(umm_t* u);
+
+int umm_layout(const umm_t* u, umm_layout_t* out);
+
+/* Current layout of the weights and of the KV cache (UMM_MODE_*).  Modes
+ * flip when a reshard is enqueued; umm_status_sync() restores the KV mode of
+ * a call that a device-detected error stopped. */
+int umm_get_modes(const umm_t* u, int32_t* weight_mode, int32_t* kv_mode);
+
+/* Declare which layout the data is in (e.g. after the caller loaded it). */
+int umm_set_modes(umm_t* u, int32_t weight_mode, int32_t kv_mode);
+
+/* §3.1, §4.2, §4.3: expert weights EP -> TP, in place, layers ascending (one
+ * launch per layer): EP slot l+1 of every region -> TP slot l of every
+ * region.  W13 row j = g*I + i of EP expert (r, e_l) goes to TP rank i / (I/P),
+ * expert r*E/P + e_l, row g*I/P + i % (I/P) (w13_split 0); W2 column i goes
+ * to TP rank i / (I/P), column i % (I/P).  Errors: MODE (weights not in EP),
+ * INVALID_ARG (no weights), CUDA. */
+int reshard_weights_ep2tp(umm_t* u, void* stream);
+
+/* Inverse of the above, layers descending: TP slot l -> EP slot l+1. */
+int reshard_weights_tp2ep(umm_t* u, void* stream);
+
+/* §3.2 EP -> TP request order (metadata all-gather): the global list is rank
+ * 0's requests, then rank 1's, ..., each rank's in ascending request index.
+ * d_tp_pos[k] receives request k's position.  d_ep_owner[k] in [0, P).
+ * Device errors: BAD_REQUEST (owner out of range; d_tp_pos untouched). */
+int gather_requests_ep2tp(umm_t* u, int32_t R, const int32_t* d_ep_owner, int32_t* d_tp_pos,
+                          void* stream);
+
+/* §3.2 TP -> EP placement: requests sorted by length descending (ties: list
+ * position ascending), each to the rank with the least load so far (load =
+ * tokens; ties: lowest rank).  d_list_pos[k] = request k's position in the
+ * global list (a permutation of 0..R-1), or NULL for "position = k".
+ * Outputs d_owner[k] and d_local_pos[k] (rank of k among its owner's requests
+ * by list position).  Device errors: BAD_REQUEST (negative length or list
+ * positions not a permutation; outputs untouched). */
+int place_requests_tp2ep(umm_t* u, int32_t R, const int32_t* d_seq_lens, const int32_t* d_list_pos,
+                         int32_t* d_owner, int32_t* d_local_pos, void* stream);
+
+/* Destination pages for a switch, handed out from free lists in list order
+ * (the page's "reassigned target pages", §3.2).  Pool g's free pages are
+ * d_free_pages[g*free_stride + 0 .. free_count-1]; request k draws from pool
+ * d_pool[k] (NULL = pool 0) and requests of a pool are served in ascending
+ * d_key order (NULL = request index; keys must be a permutation of 0..R-1),
+ * each taking ceil(len/page_size) consecutive free entries.  Writes
+ * d_page_table[k*max_pages_per_req + p], -1 past the request's pages.
+ * Device errors: CAPACITY (a pool runs out), BAD_REQUEST (bad length, pool or
+ * key); on error the table is untouched. */
+int umm_assign_pages(umm_t* u, int32_t npools, int32_t R, const int32_t* d_seq_lens,
+                     const int32_t* d_pool, const int32_t* d_key, const int32_t* d_free_pages,
+                     int64_t free_stride, int64_t free_count, int32_t* d_page_table,
+                     int32_t max_pages_per_req, void* stream);
+
+/* §3.2, §4.3, Fig. 8b: paged KV EP -> TP, in place, layers ascending.
+ * Request k (length d_seq_lens[k]) is owned by EP rank d_ep_owner[k]; its
+ * logical page p sits at EP page d_ep_page_table[k*maxp + p] of that rank
+ * and goes to TP page d_tp_page_table[k*maxp + p] on every rank holding each
+ * head (TP page ids are the same on all ranks).  Token t of page p is row
+ * t % page_size.  One descriptor-building pass (validation first), then one
+ * gather/scatter launch per layer; each source row is read once and stored to
+ * every replica.  Bytes of pages past a request's length, and of unused
+ * pages, are not written.  Errors: MODE, INVALID_ARG (sync); BAD_REQUEST,
+ * CAPACITY, PAGE_OOB, DUP_PAGE (device, before any write). */
+int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
+                     const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                     const int32_t* d_tp_page_table, void* stream);
+
+/* Paged KV TP -> EP, layers descending: request k goes to its new EP owner
+ * d_ep_owner[k] (from place_requests_tp2ep), logical page p from TP page
+ * d_tp_page_table[k*maxp+p] to EP page d_ep_page_table[k*maxp+p] of that
+ * owner; each head is read from the lowest TP rank holding it. */
+int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
+                     const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                     const int32_t* d_tp_page_table, void* stream);
+
+/* §4.5 capacity check on the host, before committing a switch: UMM_OK if the
+ * target layout's KV pools hold the requests (TP: all pages in one pool of
+ * pages_tp; EP: each owner's pages within pages_ep), else UMM_ERR_CAPACITY.
+ * h_ep_owner is needed for target UMM_MODE_EP only. */
+int umm_kv_check_capacity(const umm_t* u, int32_t target_kv_mode, int32_t R,
+                          const int32_t* h_seq_lens, const int32_t* h_ep_owner);
+
+/* Synchronise `stream`, read the sticky device flags, clear them, and return
+ * the highest-priority code among them (BAD_REQUEST > CAPACITY > PAGE_OOB >
+ * DUP_PAGE; UMM_OK if none) in *status_out (flags in *flags_out, may be
+ * NULL).  If a KV reshard was stopped, the handle's KV mode is set back to
+ * the layout the data is actually in. */
+int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags_out);
+
+/* Static description of a status code. */
+const char* umm_strerror(int code);
+
+/* Per-kernel timing with CUDA events recorded on the launching stream
+ * (diagnostics; not for use under graph capture).  Kinds: */
+#define UMM_K_WEIGHTS_EP2TP 0
+#define UMM_K_WEIGHTS_TP2EP 1
+#define UMM_K_KV_PREP       2
+#define UMM_K_KV_EP2TP      3
+#define UMM_K_KV_TP2EP      4
+#define UMM_K_PLACE         5
+#define UMM_K_ORDER         6
+#define UMM_K_ASSIGN        7
+#define UMM_K_COUNT         8
+int umm_profile_enable(umm_t* u, int32_t enable);
+/* Synchronises the recorded events; launches and summed milliseconds of one
+ * kind since the last reset. */
+int umm_profile_read(umm_t* u, int32_t kind, int64_t* launches, double* total_ms);
+int umm_profile_reset(umm_t* u);
+
+/* Number of kernels this handle has enqueued since umm_create (counted on
+ * the host at launch time). */
+int umm_launch_count(const umm_t* u, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UMM_H_ */

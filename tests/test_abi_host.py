@@ -1,0 +1,131 @@
+"""Host-side checks of the C-ABI library (no GPU): it loads, exports every
+entry point include/umm.h declares, and its host logic (layout, argument
+checks, capacity check, status strings) agrees with the header and with the
+oracle's independent layout computation."""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import oracle
+from ep_tp_weight_gb300 import build as umm_build
+from helpers import dims_of
+from synth.workloads import ALL, TINY, Workload
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "umm.h"
+
+
+@pytest.fixture(scope="module")
+def umm():
+    umm_build.build()
+    import ep_tp_weight_gb300 as m
+    return m
+
+
+def declared_functions() -> list[str]:
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def header_defines() -> dict[str, int]:
+    return {m.group(1): int(m.group(2), 0) for m in
+            re.finditer(r"#define\s+(UMM_\w+)\s+(0x[0-9a-fA-F]+|\d+)u?", HEADER.read_text())}
+
+
+def test_library_exports_every_declared_entry_point(umm):
+    names = declared_functions()
+    assert len(names) >= 20
+    lib = ctypes.CDLL(umm.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(umm.EXPORTED)
+
+
+def test_binding_constants_match_header(umm):
+    d = header_defines()
+    for k, v in d.items():
+        if k.startswith(("UMM_ERR_", "UMM_MODE_", "UMM_OK")):
+            assert getattr(umm, k) == v, k
+        if k.startswith("UMM_FLAG_"):
+            assert getattr(umm, k.replace("UMM_", "")) == v, k
+        if k.startswith("UMM_K_") and k != "UMM_K_COUNT":
+            assert getattr(umm, k.replace("UMM_", "")) == v, k
+    # the oracle restates the same flag bits on its own
+    assert (oracle.F_BAD_REQUEST, oracle.F_CAPACITY, oracle.F_PAGE_OOB, oracle.F_DUP_PAGE) == \
+        (d["UMM_FLAG_BAD_REQUEST"], d["UMM_FLAG_CAPACITY"], d["UMM_FLAG_PAGE_OOB"], d["UMM_FLAG_DUP_PAGE"])
+
+
+def test_struct_sizes_match_c_abi(umm):
+    assert ctypes.sizeof(umm.UmmDims) == 64
+    assert ctypes.sizeof(umm.UmmLayout) == 128
+
+
+def lib_dims(umm, w: Workload, **over):
+    d = w.dims()
+    d.update(over)
+    return umm.make_dims(P=d["P"], E=d["E"], H=d["H"], I=d["I"], N=d["N"], Hkv=d["Hkv"], D=d["D"],
+                         ps=d["ps"], pages_tp=d["pages_tp"], max_requests=d["max_requests"],
+                         max_pages=d["max_pages"], w13_split=d["w13_split"])
+
+
+@pytest.mark.parametrize("name", sorted(ALL))
+def test_layout_matches_oracle(umm, name):
+    w = ALL[name]
+    L = umm.umm_layout_for_dims(lib_dims(umm, w))
+    O = oracle.layout(dims_of(w))
+    for k in ("region_stride", "wslot_stride", "w13_off", "w2_off", "kvslot_stride", "kv_v_off",
+              "kvslots_off", "ws_off", "pages_ep", "pages_tp", "h_tp"):
+        assert L[k] == O[k], (name, k)
+    assert umm.umm_required_bytes(lib_dims(umm, w)) == L["total_bytes"] > L["ws_off"]
+    assert L["status_off"] == L["ws_off"] and L["desc_off"] % 256 == 0
+
+
+def test_layout_variants_match_oracle(umm):
+    for w in (TINY.with_(Hkv=4, P=2), TINY.with_(Hkv=1, P=4, E=8, I=32), TINY.with_(E=0),
+              TINY.with_(Hkv=0), Workload("odd", P=3, N=2, E=6, H=7, I=9, Hkv=6, D=5, ps=3, R=3,
+                                          len_a=1, len_b=10)):
+        L = umm.umm_layout_for_dims(lib_dims(umm, w))
+        O = oracle.layout(dims_of(w))
+        assert all(L[k] == O[k] for k in O), w.name
+
+
+def test_full_switch_fits_one_gb300(umm):
+    """The full-switch workload (weights of 128 experts x 8 layers + KV of
+    2048 requests) must fit in 284,208 MiB with room for the CUDA context."""
+    from synth.workloads import FULL_SWITCH
+    need = umm.umm_required_bytes(lib_dims(umm, FULL_SWITCH))
+    assert need < 270 * 2**30
+
+
+@pytest.mark.parametrize("bad", [dict(P=0), dict(E=9), dict(I=31), dict(Hkv=3), dict(pages_tp=3),
+                                 dict(D=0), dict(ps=0), dict(w13_split=2), dict(P=65, E=0, Hkv=0),
+                                 dict(max_requests=-1)])
+def test_bad_dims_rejected(umm, bad):
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_required_bytes(lib_dims(umm, TINY, **bad))
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+
+
+def test_null_handle_and_strerror(umm):
+    for code in range(0, 10):
+        assert umm.strerror(code) and umm.strerror(code) != "unknown status"
+    assert umm.strerror(99) == "unknown status"
+    lib = ctypes.CDLL(umm.LIB_PATH)
+    lib.reshard_weights_ep2tp.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.reshard_weights_ep2tp(None, None) == umm.UMM_ERR_INVALID_ARG
+    lib.umm_status_sync.argtypes = [ctypes.c_void_p] * 4
+    assert lib.umm_status_sync(None, None, None, None) == umm.UMM_ERR_INVALID_ARG
+
+
+def test_create_rejects_misaligned_and_small_buffers(umm):
+    d = lib_dims(umm, TINY)
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_create(d, 0x1000 + 8, 1 << 30)
+    assert ei.value.code == umm.UMM_ERR_ALIGN
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_create(d, 0x100000, 16)
+    assert ei.value.code == umm.UMM_ERR_CAPACITY

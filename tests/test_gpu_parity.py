@@ -1,0 +1,302 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by
+element on whole buffers, at sizes the oracle finishes in seconds that still
+span many tiles and ragged tails; plus error paths, address stability and
+CUDA-graph capture.  Tolerance 0: the method is pure data movement."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import ep_tp_weight_gb300 as umm
+import oracle
+import synth
+from gpu_helpers import DevUMM, i32
+from helpers import initial_kv_state
+from synth.workloads import TINY, Workload
+
+pytestmark = pytest.mark.gpu
+
+# weights: 16 B vectors, 8 B vectors (I/P = 12), 4 B (I/P = 6), 2 B (odd H); split 1
+W_CASES = [
+    TINY,
+    Workload("w_v8_ragged", P=4, N=3, E=8, H=200, I=48, w_sigma=0.02),
+    Workload("w_v4", P=2, N=2, E=4, H=36, I=12),
+    Workload("w_v2_oddh", P=3, N=2, E=6, H=35, I=9),
+    Workload("w_p1", P=1, N=3, E=3, H=64, I=40),
+    Workload("w_p8_tiles", P=8, N=2, E=16, H=256, I=128, w_sigma=0.02),
+]
+
+KV_CASES = [
+    TINY,
+    Workload("kv_hkv2_p4", P=4, N=3, Hkv=2, D=8, ps=4, R=9, len_a=1, len_b=23),
+    Workload("kv_hkv8_p4_d12", P=4, N=2, Hkv=8, D=12, ps=5, R=13, len_a=1, len_b=41),
+    Workload("kv_hkv1_p4_d5", P=4, N=2, Hkv=1, D=5, ps=3, R=7, len_a=1, len_b=20),
+    Workload("kv_hkv4_p8_d128", P=8, N=2, Hkv=4, D=128, ps=16, R=40, len_a=1, len_b=300, kv_sigma=1.0),
+    Workload("kv_hkv4_p4_many_pages", P=4, N=2, Hkv=4, D=16, ps=8, R=300, len_a=1, len_b=200),
+]
+
+
+@pytest.fixture(autouse=True)
+def _built():
+    from ep_tp_weight_gb300 import build
+    build.build()
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("w", W_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("split", [0, 1])
+def test_weights_full_buffer_parity(w, split):
+    dev = DevUMM(w, seed=3, w13_split=split)
+    d = oracle.Dims(**{**w.dims(), "w13_split": split})
+    ref = dev.host()
+    umm.reshard_weights_ep2tp(dev.h)
+    oracle.weights_ep2tp(ref, d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    assert umm.umm_get_modes(dev.h)[0] == umm.UMM_MODE_TP
+    umm.reshard_weights_tp2ep(dev.h)
+    oracle.weights_tp2ep(ref, d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
+
+
+def _kv_round(dev: DevUMM, w: Workload):
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=5)
+    ref = dev.host()
+    g = lambda a: i32(a)
+    lens, owner, ep_pt, tp_pt = g(st.lens), g(st.owner), g(st.ep_pt), g(st.tp_pt)
+    maxp = st.ep_pt.shape[1]
+    umm.reshard_kv_ep2tp(dev.h, len(st.lens), maxp, lens, owner, ep_pt, tp_pt)
+    assert oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    # a6 parity: the descriptors in the workspace
+    nd = int(synth.npages(st.lens, d.ps).sum())
+    want = oracle.kv_descriptors(d, 0, st.lens, st.owner, st.ep_pt, st.tp_pt)
+    got = dev.buf[L["desc_off"]:L["desc_off"] + 32 * nd].view(torch.int32).reshape(nd, 8).cpu().numpy()
+    np.testing.assert_array_equal(got, want)
+    # TP -> EP with the greedy placement and new pages
+    owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+    free2 = synth.permutation(8, 4, L["pages_ep"], rows=d.P)
+    fl, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, maxp, free2, region=owner2, key=st.tp_pos)
+    assert fl == 0
+    umm.reshard_kv_tp2ep(dev.h, len(st.lens), maxp, lens, g(owner2), g(ep_pt2), tp_pt)
+    assert oracle.kv_tp2ep(ref, d, st.lens, owner2, ep_pt2, st.tp_pt) == 0
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    want = oracle.kv_descriptors(d, 1, st.lens, owner2, ep_pt2, st.tp_pt)
+    got = dev.buf[L["desc_off"]:L["desc_off"] + 32 * nd].view(torch.int32).reshape(nd, 8).cpu().numpy()
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("w", KV_CASES, ids=lambda w: w.name)
+def test_kv_full_buffer_parity(w):
+    dev = DevUMM(w, seed=4)
+    _kv_round(dev, w)
+    dev.close()
+
+
+def test_weights_and_kv_together_and_modes():
+    w = TINY
+    dev = DevUMM(w, seed=9)
+    _kv_round(dev, w)
+    ref = dev.host()
+    umm.reshard_weights_ep2tp(dev.h)
+    oracle.weights_ep2tp(ref, dev.d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    with pytest.raises(umm.UmmError) as ei:
+        umm.reshard_weights_ep2tp(dev.h)
+    assert ei.value.code == umm.UMM_ERR_MODE
+    with pytest.raises(umm.UmmError) as ei:
+        umm.reshard_kv_tp2ep(dev.h, 0, 1, None, None, None, None)
+    assert ei.value.code == umm.UMM_ERR_MODE
+    dev.close()
+
+
+# ------------------------------------------------------------------ request metadata
+
+@pytest.mark.parametrize("P,R", [(2, 4), (8, 2048), (3, 1), (8, 5000), (16, 300), (5, 20000), (64, 100)])
+def test_order_place_assign_parity(P, R):
+    rng = np.random.default_rng(P * 1000 + R)
+    lens = synth.lengths_lognormal(R, R, 2048, 1.0, 32768) if R > 50 else rng.integers(1, 60, R).astype(np.int32)
+    if R > 100:
+        lens[rng.integers(0, R, R // 10)] = 77      # many equal lengths: tie-breaks matter
+    ps = 16
+    maxp = int((lens.max() + ps - 1) // ps)
+    w = Workload("meta", P=P, N=1, Hkv=P, D=8, ps=ps, R=R, len_a=1, len_b=1)
+    pages_tp = (int(synth.npages(lens, ps).sum()) + 7 + P - 1) // P * P
+    dev = DevUMM(w, fill=False, pages_tp=pages_tp, max_requests=R, max_pages=pages_tp)
+    owner0 = rng.integers(0, P, R).astype(np.int32)
+    dl, do = i32(lens), i32(owner0)
+    tp_pos = torch.empty(R, dtype=torch.int32, device="cuda")
+    umm.gather_requests_ep2tp(dev.h, R, do, tp_pos)
+    want_pos = oracle.request_order(P, owner0)
+    assert np.array_equal(tp_pos.cpu().numpy(), want_pos)
+    owner = torch.empty(R, dtype=torch.int32, device="cuda")
+    local = torch.empty(R, dtype=torch.int32, device="cuda")
+    for key in (None, tp_pos):
+        umm.place_requests_tp2ep(dev.h, R, dl, key, owner, local)
+        wo, wl, _ = oracle.place(P, lens, None if key is None else want_pos)
+        assert np.array_equal(owner.cpu().numpy(), wo)
+        assert np.array_equal(local.cpu().numpy(), wl)
+    # pages: one pool in list order, and per-rank pools in local order
+    free = synth.permutation(1, 3, pages_tp, rows=1)
+    pt = torch.full((R, maxp), -9, dtype=torch.int32, device="cuda")
+    umm.umm_assign_pages(dev.h, 1, R, dl, None, tp_pos, i32(free), pages_tp, pages_tp, pt, maxp)
+    fl, want = oracle.assign_pages(1, lens, ps, maxp, free, key=want_pos)
+    assert fl == 0 and np.array_equal(pt.cpu().numpy(), want)
+    n_ep = pages_tp                                  # generous per-rank free lists
+    free_ep = synth.permutation(2, 4, n_ep, rows=P)
+    wo, _, _ = oracle.place(P, lens, want_pos)
+    fl, want = oracle.assign_pages(P, lens, ps, maxp, free_ep, region=wo, key=want_pos)
+    umm.umm_assign_pages(dev.h, P, R, dl, i32(wo), tp_pos, i32(free_ep), n_ep, n_ep, pt, maxp)
+    st = dev.status()
+    if fl == 0:
+        assert st == (0, 0) and np.array_equal(pt.cpu().numpy(), want)
+    else:
+        assert st[0] == umm.UMM_ERR_CAPACITY
+    dev.close()
+
+
+def test_empty_and_degenerate_requests():
+    w = Workload("deg", P=4, N=2, Hkv=4, D=8, ps=4, R=3, len_a=0, len_b=0)
+    dev = DevUMM(w, seed=1, pages_tp=8, max_requests=8, max_pages=8)
+    ref = dev.host()
+    z = torch.zeros(0, dtype=torch.int32, device="cuda")
+    umm.reshard_kv_ep2tp(dev.h, 0, 1, z, z, z, z)              # R = 0: nothing moves
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    lens = np.array([0, 0, 0], np.int32)                      # zero-length requests
+    pt = np.full((3, 2), -1, np.int32)
+    umm.reshard_kv_tp2ep(dev.h, 3, 2, i32(lens), i32([0, 1, 2]), i32(pt), i32(pt))
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
+
+
+# ------------------------------------------------------------------ error paths (all-or-nothing)
+
+def test_kv_device_errors_leave_buffer_untouched():
+    w = KV_CASES[1]
+    dev = DevUMM(w, seed=2)
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=5)
+    ref = dev.host()
+    maxp = st.ep_pt.shape[1]
+    cases = []
+    bad = st.ep_pt.copy(); bad[0, 0] = L["pages_ep"]; cases.append(("ep_pt", bad, umm.UMM_ERR_PAGE_OOB))
+    bad = st.tp_pt.copy(); bad[0, 0] = -1; cases.append(("tp_pt", bad, umm.UMM_ERR_PAGE_OOB))
+    k2 = int(np.argmax(st.lens > d.ps))
+    bad = st.tp_pt.copy(); bad[k2, 1] = bad[0, 0]; cases.append(("tp_pt", bad, umm.UMM_ERR_DUP_PAGE))
+    bad = st.lens.copy(); bad[1] = -3; cases.append(("lens", bad, umm.UMM_ERR_BAD_REQUEST))
+    bad = st.owner.copy(); bad[2] = d.P; cases.append(("owner", bad, umm.UMM_ERR_BAD_REQUEST))
+    for name, arr, code in cases:
+        a = dict(lens=st.lens, owner=st.owner, ep_pt=st.ep_pt, tp_pt=st.tp_pt)
+        a[name] = arr
+        want = oracle.kv_validate(d, 0, a["lens"], a["owner"], a["ep_pt"], a["tp_pt"])
+        umm.reshard_kv_ep2tp(dev.h, len(st.lens), maxp, i32(a["lens"]), i32(a["owner"]), i32(a["ep_pt"]),
+                             i32(a["tp_pt"]))
+        assert umm.umm_get_modes(dev.h)[1] == umm.UMM_MODE_TP      # flipped at enqueue ...
+        code_got, flags = dev.status()
+        assert (code_got, flags) == (code, want), name
+        assert umm.umm_get_modes(dev.h)[1] == umm.UMM_MODE_EP      # ... restored by the sync
+        np.testing.assert_array_equal(dev.host(), ref)
+    # sticky: a failed page hand-out stops the following KV call too
+    big = np.full(len(st.lens), 10**6, np.int32)
+    pt = torch.zeros(st.tp_pt.shape, dtype=torch.int32, device="cuda")
+    umm.umm_assign_pages(dev.h, 1, len(st.lens), i32(big), None, None, i32(np.arange(4)), 4, 4, pt, maxp)
+    umm.reshard_kv_ep2tp(dev.h, len(st.lens), maxp, i32(st.lens), i32(st.owner), i32(st.ep_pt), i32(st.tp_pt))
+    assert dev.status()[0] == umm.UMM_ERR_BAD_REQUEST
+    np.testing.assert_array_equal(dev.host(), ref)
+    assert umm.umm_get_modes(dev.h)[1] == umm.UMM_MODE_EP
+    # capacity: more pages than the TP pool
+    small = DevUMM(w, seed=2, pages_tp=int(synth.npages(st.lens, d.ps).sum()) // 2 // 2 * 2)
+    ref2 = small.host()
+    umm.reshard_kv_ep2tp(small.h, len(st.lens), maxp, i32(st.lens), i32(st.owner),
+                         i32(np.zeros_like(st.ep_pt)), i32(st.tp_pt))
+    assert small.status()[0] == umm.UMM_ERR_CAPACITY
+    np.testing.assert_array_equal(small.host(), ref2)
+    assert umm.umm_kv_check_capacity(small.h, umm.UMM_MODE_TP, len(st.lens), st.lens) == umm.UMM_ERR_CAPACITY
+    assert umm.umm_kv_check_capacity(dev.h, umm.UMM_MODE_TP, len(st.lens), st.lens) == umm.UMM_OK
+    small.close()
+    dev.close()
+
+
+# ------------------------------------------------------------------ fixed addresses, graphs, no allocation
+
+def test_address_stability_graph_replay_and_no_allocation():
+    """§4.2: tensors keep their addresses across switches, so a CUDA graph
+    captured on the TP views before any switch reads the right data after
+    EP->TP->EP->TP; and the switch path allocates no device memory."""
+    w = Workload("gr", P=4, N=2, E=8, H=64, I=32, Hkv=4, D=16, ps=4, R=6, len_a=1, len_b=30)
+    dev = DevUMM(w, seed=6)
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=1)
+    ref = dev.host()
+    maxp = st.ep_pt.shape[1]
+    lens, owner, ep_pt, tp_pt = i32(st.lens), i32(st.owner), i32(st.ep_pt), i32(st.tp_pt)
+    # probe graph: copy TP slot 0 of every region (weights + KV) into a probe buffer
+    spans = [(r * L["region_stride"], L["wslot_stride"]) for r in range(d.P)] + \
+            [(r * L["region_stride"] + L["kvslots_off"], L["kvslot_stride"]) for r in range(d.P)]
+    probe = torch.empty(sum(n for _, n in spans), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    views = [dev.buf[a:a + n] for a, n in spans]
+    ptrs = [v.data_ptr() for v in views]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            torch.cat(views, out=probe)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    cur = torch.cuda.current_stream()
+    owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+    free2 = synth.permutation(8, 4, L["pages_ep"], rows=d.P)
+    _, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, maxp, free2, region=owner2, key=st.tp_pos)
+    o2, e2 = i32(owner2), i32(ep_pt2)
+    # EP -> TP -> EP -> TP, on the current stream, no allocation in between
+    umm.reshard_weights_ep2tp(dev.h, cur); umm.reshard_kv_ep2tp(dev.h, len(st.lens), maxp, lens, owner, ep_pt, tp_pt, cur)
+    umm.reshard_weights_tp2ep(dev.h, cur); umm.reshard_kv_tp2ep(dev.h, len(st.lens), maxp, lens, o2, e2, tp_pt, cur)
+    umm.reshard_weights_ep2tp(dev.h, cur); umm.reshard_kv_ep2tp(dev.h, len(st.lens), maxp, lens, o2, e2, tp_pt, cur)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert dev.status() == (0, 0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert [v.data_ptr() for v in views] == ptrs
+    oracle.weights_ep2tp(ref, d); oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, st.tp_pt)
+    oracle.weights_tp2ep(ref, d); oracle.kv_tp2ep(ref, d, st.lens, owner2, ep_pt2, st.tp_pt)
+    oracle.weights_ep2tp(ref, d); oracle.kv_ep2tp(ref, d, st.lens, owner2, ep_pt2, st.tp_pt)
+    want = np.concatenate([ref[a:a + n] for a, n in spans])
+    np.testing.assert_array_equal(probe.cpu().numpy(), want)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
+
+
+def test_switch_captured_in_a_cuda_graph():
+    """The switch itself enqueues only kernels on the given stream, so a whole
+    EP->TP switch (weights + KV) can be captured once and replayed."""
+    w = Workload("cap", P=4, N=2, E=8, H=64, I=32, Hkv=2, D=16, ps=4, R=5, len_a=1, len_b=25)
+    dev = DevUMM(w, seed=7)
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=2)
+    maxp = st.ep_pt.shape[1]
+    lens, owner, ep_pt, tp_pt = i32(st.lens), i32(st.owner), i32(st.ep_pt), i32(st.tp_pt)
+    ref = dev.host()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            umm.reshard_weights_ep2tp(dev.h, s)
+            umm.reshard_kv_ep2tp(dev.h, len(st.lens), maxp, lens, owner, ep_pt, tp_pt, s)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dev.host(), ref)        # capture ran nothing
+    g.replay()
+    torch.cuda.synchronize()
+    oracle.weights_ep2tp(ref, d)
+    oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, st.tp_pt)
+    np.testing.assert_array_equal(dev.host(), ref)
+    assert dev.status() == (0, 0)
+    dev.close()
