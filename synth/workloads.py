@@ -91,4 +91,10 @@ FULL_SWITCH = Workload("full_switch_p8_e128_h2048_i768_8layers_2048req_lognormal
                        len_kind="lognormal", len_a=2048, len_b=1.0, len_cap=32768,
                        w_sigma=0.02, kv_sigma=1.0)
 
-ALL = {w.name: w for w in (TINY, WEIGHTS_H2048, WEIGHTS_H4096, KV_256REQ, FULL_SWITCH)}
+# Small cases of the same kernels for ncu captures (a few GB on the device,
+# per-launch traffic still far above the 129 MB L2).
+KV_PROFILE = KV_256REQ.with_(name="kv_p8_2layers_8req_u1k-32k_hkv4_d128", N=2, R=8)
+WEIGHTS_PROFILE = WEIGHTS_H2048.with_(name="weights_p8_e128_h2048_i768_2layers", N=2)
+
+ALL = {w.name: w for w in (TINY, WEIGHTS_H2048, WEIGHTS_H4096, KV_256REQ, FULL_SWITCH, KV_PROFILE,
+                           WEIGHTS_PROFILE)}

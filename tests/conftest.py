@@ -10,6 +10,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300)")
+    # compile the native parts if they are missing or stale (nvcc and gcc
+    # work without a GPU); the package import fails loudly without them
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 def pytest_collection_modifyitems(config, items):

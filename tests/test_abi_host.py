@@ -12,7 +12,6 @@ import numpy as np
 import pytest
 
 import oracle
-from ep_tp_weight_gb300 import build as umm_build
 from helpers import dims_of
 from synth.workloads import ALL, TINY, Workload
 
@@ -21,7 +20,6 @@ HEADER = Path(__file__).resolve().parent.parent / "include" / "umm.h"
 
 @pytest.fixture(scope="module")
 def umm():
-    umm_build.build()
     import ep_tp_weight_gb300 as m
     return m
 

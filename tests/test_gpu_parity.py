@@ -30,7 +30,7 @@ W_CASES = [
 KV_CASES = [
     TINY,
     Workload("kv_hkv2_p4", P=4, N=3, Hkv=2, D=8, ps=4, R=9, len_a=1, len_b=23),
-    Workload("kv_hkv8_p4_d12", P=4, N=2, Hkv=8, D=12, ps=5, R=13, len_a=1, len_b=41),
+    Workload("kv_hkv8_p4_d12", P=4, N=2, Hkv=8, D=12, ps=5, R=13, len_a=1, len_b=41, slack=2.0),
     Workload("kv_hkv1_p4_d5", P=4, N=2, Hkv=1, D=5, ps=3, R=7, len_a=1, len_b=20),
     Workload("kv_hkv4_p8_d128", P=8, N=2, Hkv=4, D=128, ps=16, R=40, len_a=1, len_b=300, kv_sigma=1.0),
     Workload("kv_hkv4_p4_many_pages", P=4, N=2, Hkv=4, D=16, ps=8, R=300, len_a=1, len_b=200),
@@ -38,9 +38,7 @@ KV_CASES = [
 
 
 @pytest.fixture(autouse=True)
-def _built():
-    from ep_tp_weight_gb300 import build
-    build.build()
+def _sync():
     yield
     torch.cuda.synchronize()
 
