@@ -154,7 +154,12 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- traffic from committed ncu summary
 
 KERNEL_SOURCES = {"kv_copy_ep2tp": "ep_tp_weight_gb300/csrc/umm_kv.cu",
+                  "kv_copy_tp2ep": "ep_tp_weight_gb300/csrc/umm_kv.cu",
                   "weights_kernel": "ep_tp_weight_gb300/csrc/umm_weights.cu"}
+# the ncu capture (small case of the same kernel) each traffic figure comes from
+PROFILE_CASES = {"kv_copy_ep2tp": "kv_p8_2layers_8req_u1k-32k_hkv4_d128",
+                 "kv_copy_tp2ep": "kv_p8_2layers_8req_u1k-32k_hkv4_d128",
+                 "weights_kernel": "weights_p8_e128_h2048_i768_2layers"}
 
 
 def source_digest(rel: str) -> str:
@@ -162,18 +167,26 @@ def source_digest(rel: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, scaled to this
-    workload's launch size, or None when the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.md")
-    if not os.path.exists(path):
+def committed_traffic(kernel: str, units: dict):
+    """DRAM bytes per launch from the committed ncu summary of a small case of
+    the same kernel, scaled by the units one launch of this workload moves
+    (live tokens for KV, bytes for weights); None when the kernel source has
+    changed since the capture."""
+    case = PROFILE_CASES.get(kernel)
+    path = os.path.join(ROOT, "profiles", f"{kernel}.{case}.md")
+    if not case or not os.path.exists(path):
         return None
     txt = open(path).read()
     m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
-    if not m_src or not m_tr or m_src.group(1) != source_digest(KERNEL_SOURCES[kernel]):
+    if not m_src or m_src.group(1) != source_digest(KERNEL_SOURCES[kernel]):
         return None
-    return int(m_tr.group(1))
+    m_tok = re.search(r"dram_bytes_per_live_token:\s*([\d.]+)", txt)
+    m_byte = re.search(r"dram_bytes_per_algorithmic_byte:\s*([\d.]+)", txt)
+    if m_tok and units.get("tokens"):
+        return int(float(m_tok.group(1)) * units["tokens"])
+    if m_byte and units.get("bytes"):
+        return int(float(m_byte.group(1)) * units["bytes"])
+    return None
 
 
 # ----------------------------------------------------------------------------- the GPU run
@@ -496,8 +509,10 @@ def main():
                         "weights_ep2tp": b.get("weights_per_layer", 0),
                         "weights_tp2ep": b.get("weights_per_layer", 0)}.get(dom, 0)
     achieved = per_launch_bytes / (ms_dom / n_dom / 1e3) / 1e9 if n_dom else 0.0
-    kernel_name = {"kv_ep2tp": "kv_copy_ep2tp", "weights_ep2tp": "weights_kernel"}.get(dom)
-    traffic = committed_traffic(kernel_name, r["w"].name) if kernel_name else None
+    kernel_name = {"kv_ep2tp": "kv_copy_ep2tp", "kv_tp2ep": "kv_copy_tp2ep", "weights_ep2tp": "weights_kernel",
+                   "weights_tp2ep": "weights_kernel"}.get(dom)
+    traffic = committed_traffic(kernel_name, {"tokens": b.get("tokens"), "bytes": per_launch_bytes}) \
+        if kernel_name else None
     per_kind = {k: {"launches": n, "ms_per_launch": round(ms / n, 4) if n else None}
                 for k, (n, ms) in prof.items() if n}
     for k, key in (("weights_ep2tp", "weights_per_layer"), ("weights_tp2ep", "weights_per_layer"),

@@ -228,7 +228,7 @@ def test_address_stability_graph_replay_and_no_allocation():
     """§4.2: tensors keep their addresses across switches, so a CUDA graph
     captured on the TP views before any switch reads the right data after
     EP->TP->EP->TP; and the switch path allocates no device memory."""
-    w = Workload("gr", P=4, N=2, E=8, H=64, I=32, Hkv=4, D=16, ps=4, R=6, len_a=1, len_b=30)
+    w = Workload("gr", P=4, N=2, E=8, H=64, I=32, Hkv=4, D=16, ps=4, R=6, len_a=1, len_b=30, slack=3.0)
     dev = DevUMM(w, seed=6)
     d, L = dev.d, dev.L
     st = initial_kv_state(w, d, L, seed=1)
@@ -275,7 +275,7 @@ def test_address_stability_graph_replay_and_no_allocation():
 def test_switch_captured_in_a_cuda_graph():
     """The switch itself enqueues only kernels on the given stream, so a whole
     EP->TP switch (weights + KV) can be captured once and replayed."""
-    w = Workload("cap", P=4, N=2, E=8, H=64, I=32, Hkv=2, D=16, ps=4, R=5, len_a=1, len_b=25)
+    w = Workload("cap", P=4, N=2, E=8, H=64, I=32, Hkv=2, D=16, ps=4, R=5, len_a=1, len_b=25, slack=3.0)
     dev = DevUMM(w, seed=7)
     d, L = dev.d, dev.L
     st = initial_kv_state(w, d, L, seed=2)
