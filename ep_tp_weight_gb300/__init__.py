@@ -91,6 +91,7 @@ _SIG = {
     "umm_profile_read": [_vp, _i32, _P(_i64), _P(ctypes.c_double)],
     "umm_profile_reset": [_vp],
     "umm_launch_count": [_vp, _P(_i64)],
+    "place_requests_tp2ep_noalloc": [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp],
 }
 for _name, _args in _SIG.items():
     _f = getattr(_lib, _name)
@@ -189,6 +190,14 @@ def gather_requests_ep2tp(h: int, R: int, ep_owner, tp_pos, stream=None) -> None
 def place_requests_tp2ep(h: int, R: int, seq_lens, list_pos, owner, local_pos, stream=None) -> None:
     _ck(_lib.place_requests_tp2ep(h, R, _ptr(seq_lens), _ptr(list_pos), _ptr(owner), _ptr(local_pos),
                                   _stream(stream)), "place_requests_tp2ep")
+
+
+def place_requests_tp2ep_noalloc(P: int, R: int, seq_lens, list_pos, owner, local_pos, status=None,
+                                 stream=None) -> None:
+    """place_requests_tp2ep without a handle and without any allocation (for
+    callers that cannot allocate device memory); R <= 16384."""
+    _ck(_lib.place_requests_tp2ep_noalloc(P, R, _ptr(seq_lens), _ptr(list_pos), _ptr(owner), _ptr(local_pos),
+                                          _ptr(status), _stream(stream)), "place_requests_tp2ep_noalloc")
 
 
 def umm_assign_pages(h: int, npools: int, R: int, seq_lens, pool, key, free_pages, free_stride: int,

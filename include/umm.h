@@ -194,6 +194,30 @@ int gather_requests_ep2tp(umm_t* u, int32_t R, const int32_t* d_ep_owner, int32_
 int place_requests_tp2ep(umm_t* u, int32_t R, const int32_t* d_seq_lens, const int32_t* d_list_pos,
                          int32_t* d_owner, int32_t* d_local_pos, void* stream);
 
+/* The placement above, for callers that cannot allocate device memory.
+ * (The paper has no counterpart: this entry point exists for deployments.)
+ * place_requests_tp2ep() needs a handle, and the handle needs a unified
+ * buffer that someone cudaMalloc'ed.  A scheduler process that only receives
+ * device pointers to request metadata, or code running where an allocator must
+ * not be entered (inside allocator callbacks, under a strict memory budget,
+ * while other work is being captured), cannot provide one.  This variant takes
+ * no handle and allocates nothing: its scratch (the list-position -> request
+ * map) is a fixed 64 KiB array of this library's own device memory, which
+ * every GPU that loads the library reserves until the process exits.
+ *  - P in [1, 64]; R in [0, 16384]: a larger R is refused with
+ *    UMM_ERR_CAPACITY before anything is enqueued.
+ *  - Same arguments and results as place_requests_tp2ep(); d_status (device
+ *    int32, may be NULL) receives UMM_OK or UMM_ERR_BAD_REQUEST (negative
+ *    length, or list positions that are not a permutation; outputs are then
+ *    untouched).  With R == 0 nothing is enqueued and d_status is not written.
+ *  - All calls on one GPU share the scratch array: calls whose kernels may
+ *    overlap on the GPU (unordered streams) race; order them on one stream.
+ *  - The first call on each device looks up the array's address and sets the
+ *    kernel's shared-memory limit (no allocation); make that call before any
+ *    stream capture. */
+int place_requests_tp2ep_noalloc(int32_t P, int32_t R, const int32_t* d_seq_lens, const int32_t* d_list_pos,
+                                 int32_t* d_owner, int32_t* d_local_pos, int32_t* d_status, void* stream);
+
 /* Destination pages for a switch, handed out from free lists in list order
  * (the page's "reassigned target pages", §3.2).  Pool g's free pages are
  * d_free_pages[g*free_stride + 0 .. free_count-1]; request k draws from pool
