@@ -188,12 +188,14 @@ int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, co
   if (rc) return rc;
   u->launches += R > 0 ? 2 : 1;
   const int N = u->dims.num_layers;
+  // live pages <= min(descriptor capacity, R * pages per request): the grid
+  const int64_t max_desc = std::min<int64_t>(u->ws.desc_cap, (int64_t)R * maxp);
   for (int t = 0; t < N; ++t) {
     const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
     ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
-    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, s, u->sms));
+    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, s));
     if (rc) return rc;
-    ++u->launches;
+    if (max_desc > 0) ++u->launches;
   }
   u->kv_log.push_back(KvCall{call, u->kv_mode});
   if (u->kv_log.size() > 4096) u->kv_log.erase(u->kv_log.begin());

@@ -92,7 +92,8 @@ cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, i
 cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_t maxp,
                            const int32_t* lens, const int32_t* owner, const int32_t* ep_pt,
                            const int32_t* tp_pt, unsigned int call, cudaStream_t s, int sms);
-cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, cudaStream_t s, int sms);
+// max_desc: an upper bound on the descriptors of the call (the grid size).
+cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, cudaStream_t s);
 
 cudaError_t launch_order(const Geo& g, const Ws& w, int32_t R, const int32_t* owner, int32_t* tp_pos,
                          unsigned int call, cudaStream_t s);
