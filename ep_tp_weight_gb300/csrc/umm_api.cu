@@ -211,7 +211,7 @@ int reshard_weights(umm* u, int ep2tp, void* stream) {
   for (int t = 0; t < N; ++t) {
     const int layer = ep2tp ? t : N - 1 - t;
     ProfScope ps(u, ep2tp ? UMM_K_WEIGHTS_EP2TP : UMM_K_WEIGHTS_TP2EP, s);
-    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s, u->sms));
+    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s));
     if (rc) return rc;
     ++u->launches;
   }

@@ -87,7 +87,7 @@ struct Ws {
 };
 
 // ---- launchers (enqueue only; all arguments already validated) ----
-cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, int sms);
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s);
 
 cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_t maxp,
                            const int32_t* lens, const int32_t* owner, const int32_t* ep_pt,

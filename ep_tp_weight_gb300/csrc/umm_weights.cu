@@ -104,25 +104,21 @@ __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) 
 
 namespace {
 constexpr int kT = 256;
-constexpr int kU = 8;
+constexpr int kU = 4;
 
+// One CTA per 16 KiB tile (grid = all tiles of the layer) rather than a
+// persistent grid: the block scheduler refills each SM slot the moment a tile
+// is done, keeping more loads in flight (measured on GB300, E=128, H=2048,
+// I=768: 6.35 TB/s persistent with 8 vectors per thread -> 6.95 TB/s).
 template <int VB>
-cudaError_t run(const WParams& p, int ep2tp, cudaStream_t s, int sms) {
-  static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, weights_kernel<VB, kU, kT>, kT, 0);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-  }
-  uint32_t grid = (uint32_t)sms * (uint32_t)occ;
-  if (grid > p.tiles_total) grid = p.tiles_total;
-  if (grid == 0) return cudaSuccess;
-  weights_kernel<VB, kU, kT><<<grid, kT, 0, s>>>(p, ep2tp);
+cudaError_t run(const WParams& p, int ep2tp, cudaStream_t s) {
+  if (p.tiles_total == 0) return cudaSuccess;
+  weights_kernel<VB, kU, kT><<<p.tiles_total, kT, 0, s>>>(p, ep2tp);
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, int sms) {
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   const uint32_t El = (uint32_t)(g.E / g.P), Ip = (uint32_t)(g.I / g.P), H = (uint32_t)g.H;
   const uint32_t I = (uint32_t)g.I;
   int VB = 2;
@@ -157,10 +153,10 @@ cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, i
   p.tiles_per_region = FastDiv(tpr);
   p.split = g.w13_split;
   switch (VB) {
-    case 16: return run<16>(p, ep2tp, s, sms);
-    case 8: return run<8>(p, ep2tp, s, sms);
-    case 4: return run<4>(p, ep2tp, s, sms);
-    default: return run<2>(p, ep2tp, s, sms);
+    case 16: return run<16>(p, ep2tp, s);
+    case 8: return run<8>(p, ep2tp, s);
+    case 4: return run<4>(p, ep2tp, s);
+    default: return run<2>(p, ep2tp, s);
   }
 }
 
