@@ -57,6 +57,14 @@ class UmmLayout(ctypes.Structure):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
 
 
+class UmmPolicyParams(ctypes.Structure):
+    _fields_ = [("t_high", ctypes.c_double), ("t_low", ctypes.c_double), ("window", ctypes.c_int32),
+                ("cooldown_s", ctypes.c_double), ("start_mode", ctypes.c_int32)]
+
+
+POLICY_STAY, POLICY_TO_EP, POLICY_TO_TP, POLICY_CANCELLED = 0, 1, 2, 3
+
+
 class UmmError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
@@ -92,6 +100,10 @@ _SIG = {
     "umm_profile_reset": [_vp],
     "umm_launch_count": [_vp, _P(_i64)],
     "place_requests_tp2ep_noalloc": [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "umm_policy_create": [_vp, _P(_vp)],
+    "umm_policy_destroy": [_vp],
+    "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
+    "umm_policy_state": [_vp, _P(_i32), _P(_i64), _P(_i64)],
 }
 for _name, _args in _SIG.items():
     _f = getattr(_lib, _name)
@@ -257,3 +269,28 @@ def umm_launch_count(h: int) -> int:
     n = ctypes.c_int64()
     _ck(_lib.umm_launch_count(h, ctypes.byref(n)), "umm_launch_count")
     return n.value
+
+
+def umm_policy_create(t_high: float, t_low: float, window: int, cooldown_s: float,
+                      start_mode: int = UMM_MODE_TP) -> int:
+    h = ctypes.c_void_p()
+    prm = UmmPolicyParams(t_high, t_low, window, cooldown_s, start_mode)
+    _ck(_lib.umm_policy_create(ctypes.byref(prm), ctypes.byref(h)), "umm_policy_create")
+    return h.value
+
+
+def umm_policy_destroy(h: int) -> None:
+    _ck(_lib.umm_policy_destroy(h), "umm_policy_destroy")
+
+
+def umm_policy_step(h: int, inflight: int, now_s: float, target_fits: bool = True) -> int:
+    d = ctypes.c_int32()
+    _ck(_lib.umm_policy_step(h, int(inflight), float(now_s), 1 if target_fits else 0, ctypes.byref(d)),
+        "umm_policy_step")
+    return d.value
+
+
+def umm_policy_state(h: int) -> tuple[int, int, int]:
+    m, sw, ca = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64()
+    _ck(_lib.umm_policy_state(h, ctypes.byref(m), ctypes.byref(sw), ctypes.byref(ca)), "umm_policy_state")
+    return m.value, sw.value, ca.value

@@ -265,8 +265,11 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
 }
 
 namespace {
-constexpr int kT = 256;
-constexpr int kU = 4;
+// EP->TP: 128 threads x 8 vectors (half a 32 KiB K+V page per round);
+// TP->EP: 256 x 4.  Both picked by measurement on GB300 (within ~1% of the
+// neighbouring shapes; 16-vector-per-thread or persistent shapes were slower).
+constexpr int kT_ep2tp = 128, kU_ep2tp = 8;
+constexpr int kT_tp2ep = 256, kU_tp2ep = 4;
 
 // One CTA per descriptor (grid >= live pages): the block scheduler hands a
 // finished CTA's slot to the next page at once, which keeps more loads in
@@ -277,8 +280,8 @@ template <int VB>
 cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t s) {
   if (max_desc <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)(max_desc < 0x7fffffffll ? max_desc : 0x7fffffffll);
-  if (dir == 0) kv_copy_ep2tp<VB, kU, kT><<<grid, kT, 0, s>>>(p);
-  else kv_copy_tp2ep<VB, kU, kT><<<grid, kT, 0, s>>>(p);
+  if (dir == 0) kv_copy_ep2tp<VB, kU_ep2tp, kT_ep2tp><<<grid, kT_ep2tp, 0, s>>>(p);
+  else kv_copy_tp2ep<VB, kU_tp2ep, kT_tp2ep><<<grid, kT_tp2ep, 0, s>>>(p);
   return cudaGetLastError();
 }
 }  // namespace

@@ -292,6 +292,40 @@ int umm_profile_reset(umm_t* u);
  * the host at launch time). */
 int umm_launch_count(const umm_t* u, int64_t* launches);
 
+/* ---- switch policy (host only; §4.5, settings of §6.1) ----
+ * Decides, once per decode iteration, whether to switch layouts:
+ *  - in TP, switch to EP as soon as the latest in-flight count > t_high;
+ *  - in EP, switch to TP only when the mean of the last `window` counts is
+ *    < t_low (t_low <= t_high: hysteresis); the window holds the last
+ *    `window` samples in every mode and must be full;
+ *  - no decision for cooldown_s seconds after a switch or a cancellation;
+ *  - a wanted switch whose target layout cannot hold the live requests
+ *    (target_fits = 0, e.g. from umm_kv_check_capacity) is cancelled and
+ *    retried after the cooldown.
+ * Deterministic: the same inputs give the same decisions. */
+typedef struct {
+  double t_high, t_low;    /* thresholds on the in-flight request count       */
+  int32_t window;          /* W >= 1 iterations averaged in EP                 */
+  double cooldown_s;       /* C >= 0 seconds                                    */
+  int32_t start_mode;      /* UMM_MODE_EP or UMM_MODE_TP                        */
+} umm_policy_params;
+
+#define UMM_POLICY_STAY      0
+#define UMM_POLICY_TO_EP     1
+#define UMM_POLICY_TO_TP     2
+#define UMM_POLICY_CANCELLED 3
+
+typedef struct umm_policy umm_policy_t;
+int umm_policy_create(const umm_policy_params* params, umm_policy_t** out);
+int umm_policy_destroy(umm_policy_t* policy);
+/* One iteration: in-flight count after the step that just finished, the time
+ * (seconds, non-decreasing) and whether the layout a switch would go to holds
+ * the live requests.  *decision = UMM_POLICY_*; the policy's mode follows
+ * UMM_POLICY_TO_EP / UMM_POLICY_TO_TP. */
+int umm_policy_step(umm_policy_t* policy, int64_t inflight, double now_s, int32_t target_fits,
+                    int32_t* decision);
+int umm_policy_state(const umm_policy_t* policy, int32_t* mode, int64_t* switches, int64_t* cancels);
+
 #ifdef __cplusplus
 }
 #endif
