@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--workload", default=FULL_SWITCH.name, choices=sorted(ALL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     return ap.parse_args()
 
 
@@ -189,6 +190,26 @@ def committed_traffic(kernel: str, units: dict):
     return None
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (identity with one process); the
+    step time every rank reports is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, ms_total_max: float, world: int) -> float:
+    """Replicas: every rank moves the same bytes per step; the job's rate is
+    all ranks' bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / (ms_total_max / 1e3) / 1e9
+
+
 # ----------------------------------------------------------------------------- the GPU run
 
 def run_umm(args, rank, world, local_rank):
@@ -316,10 +337,39 @@ def run_umm(args, rank, world, local_rank):
         raise RuntimeError(f"timed steps failed: {umm.strerror(st[0])}")
     ms_ep2tp = statistics.mean(a.elapsed_time(b) for a, b, _ in ev_half)
     ms_tp2ep = statistics.mean(b.elapsed_time(c) for _, b, c in ev_half)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
+
+    # ---------------- the same round trip replayed from a CUDA graph
+    # Two steps are captured (EP state A -> B -> A), so each replay starts from
+    # the state the previous one left; the host-side modes end where they began.
+    graph = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                step()
+                step()
+        torch.cuda.synchronize()
+        g.replay()                                   # warm-up replay
+        torch.cuda.synchronize()
+        reps = max(1, args.steps // 2)
+        barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(reps):
+                g.replay()
+        g1.record(s)
+        torch.cuda.synchronize()
+        ms_g = max_over_ranks(g0.elapsed_time(g1), dev) / (2 * reps)
+        code, _ = umm.umm_status_sync(h, s)
+        if code:
+            raise RuntimeError(f"graph replay failed: {umm.strerror(code)}")
+        graph = {"ms_per_step": round(ms_g, 3), "value": round(whole_job_gbs(bytes_model["step"], 1, ms_g, world), 1),
+                 "unit": UNIT, "steps": 2 * reps}
+        del g
 
     # ---------------- end to end through the public API with host buffers
     e2e = None
@@ -363,7 +413,7 @@ def run_umm(args, rank, world, local_rank):
     umm.umm_destroy(h)
     del buf
     torch.cuda.empty_cache()
-    return dict(w=w, lens=lens_h, ms_total=ms_total, launches=launches, prof=prof, clocks=clk.summary(),
+    return dict(w=w, lens=lens_h, ms_total=ms_total, graph=graph, launches=launches, prof=prof, clocks=clk.summary(),
                 ms_ep2tp=ms_ep2tp, ms_tp2ep=ms_tp2ep, bytes=bytes_model, e2e=e2e, layout=L, nbytes=nbytes)
 
 
@@ -499,7 +549,7 @@ def main():
         return
     b = r["bytes"]
     ms_step = r["ms_total"] / args.steps
-    value = world * b["step"] * args.steps / (r["ms_total"] / 1e3) / 1e9
+    value = whole_job_gbs(b["step"], args.steps, r["ms_total"], world)
     peak, peak_kind = peaks()
     # dominant kernel = most device time in the timed region
     prof = r["prof"]
@@ -537,6 +587,7 @@ def main():
                      "peak_kind": f"{peak_kind} copy GB/s (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": per_launch_bytes},
+        "cuda_graph": r["graph"],
         "clocks": r["clocks"], "gpu_launches": r["launches"],
         "e2e": r["e2e"],
     }

@@ -81,6 +81,7 @@ struct Ws {
   uint64_t req_inv;    // int32[max_requests]   list position -> request
   uint64_t keys;       // uint64[keys_cap]      sort keys (placement)
   int64_t keys_cap;    // power of two >= max_requests
+  uint64_t choice;     // uint8[max_requests]   placement: rank per sorted position
   uint64_t bitmap;     // uint32[bitmap_words]  destination-page use bits
   int64_t bitmap_words;
   int32_t max_requests;

@@ -13,6 +13,8 @@
 // checks with warp ballots and a destination bitmap) + one gather/scatter
 // launch per layer (kv_copy).  Nothing is written to the cache unless the
 // descriptor pass raised no flag.
+#include <algorithm>
+
 #include "umm_scan.cuh"
 
 namespace uk {
@@ -24,16 +26,22 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
              const int32_t* __restrict__ owner, unsigned int call) {
   DevStatus* st = status_of(g, w);
   if (read_flags(st)) return;
-  __shared__ long long carry[kMaxGroups];
+  __shared__ long long carry[kMaxGroups];    // running page offset per region
+  __shared__ long long carry_n[kMaxGroups];  // running request count per region
   __shared__ long long warp_tot[32 * kMaxGroups];
   __shared__ unsigned long long region_pages[kMaxGroups];
+  __shared__ unsigned int region_reqs[kMaxGroups];
   __shared__ unsigned long long tokens;
   __shared__ int bad, capfail;
   const int tid = threadIdx.x, P = g.P;
-  if (tid < kMaxGroups) region_pages[tid] = 0;
+  if (tid < kMaxGroups) {
+    region_pages[tid] = 0;
+    region_reqs[tid] = 0;
+  }
   if (tid == 0) { tokens = 0; bad = 0; capfail = 0; }
   __syncthreads();
   const long long max_len = (long long)maxp * g.ps;
+  unsigned long long my_tokens = 0;
   for (int k = tid; k < R; k += blockDim.x) {
     const int len = lens[k], o = owner[k];
     if (len < 0 || (long long)len > max_len || o < 0 || o >= P) {
@@ -41,19 +49,25 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
       continue;
     }
     atomicAdd(&region_pages[o], (unsigned long long)((len + g.ps - 1) / g.ps));
-    atomicAdd(&tokens, (unsigned long long)len);
+    atomicAdd(&region_reqs[o], 1u);
+    my_tokens += (unsigned long long)len;
   }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) my_tokens += __shfl_xor_sync(0xffffffffu, my_tokens, d);
+  if ((tid & 31) == 0) atomicAdd(&tokens, my_tokens);
   __syncthreads();
   if (bad) {
     if (tid == 0) raise_flag(st, UMM_FLAG_BAD_REQUEST, call);
     return;
   }
   if (tid == 0) {
-    unsigned long long total = 0;
+    unsigned long long total = 0, nreq = 0;
     int fail = 0;
     for (int r = 0; r < P; ++r) {
       carry[r] = (long long)total;  // descriptors of region r start here
+      carry_n[r] = (long long)nreq; // and its requests in the (region, request) order
       total += region_pages[r];
+      nreq += region_reqs[r];
       if (dir == 1 && (long long)region_pages[r] > g.pages_ep) fail = 1;
     }
     if (dir == 0 && (long long)total > g.pages_tp) fail = 1;
@@ -68,8 +82,10 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
   }
   __syncthreads();
   if (capfail) return;
-  // descriptor offsets in (owning region, request) order
-  int64_t* off = reinterpret_cast<int64_t*>(g.base + w.req_off);
+  // requests in (owning region, request) order, with their first descriptor:
+  // order_req[j] = request, order_start[j] = offset (non-decreasing in j)
+  int64_t* order_start = reinterpret_cast<int64_t*>(g.base + w.req_off);
+  int32_t* order_req = reinterpret_cast<int32_t*>(g.base + w.req_inv);
   for (int base = 0; base < R; base += blockDim.x) {
     const int k = base + tid;
     long long np = 0;
@@ -78,8 +94,12 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
       np = (lens[k] + g.ps - 1) / g.ps;
       grp = owner[k];
     }
-    const long long pre = group_exclusive_scan(np, grp, P, carry, warp_tot);
-    if (k < R) off[k] = pre;
+    const long long start = group_exclusive_scan(np, grp, P, carry, warp_tot);
+    const long long j = group_exclusive_scan(k < R ? 1 : 0, grp, P, carry_n, warp_tot);
+    if (k < R) {
+      order_start[j] = start;
+      order_req[j] = k;
+    }
   }
   // clear the destination-page bitmap
   const long long bits = dir == 0 ? g.pages_tp : (long long)P * g.pages_ep;
@@ -88,47 +108,57 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
   for (long long i = tid; i < words; i += blockDim.x) bm[i] = 0u;
 }
 
+// One thread per descriptor: a binary search over the request order finds
+// the request whose run holds descriptor d (requests without pages share the
+// next request's start, so the last start <= d is the right one).
 __global__ void __launch_bounds__(256)
 kv_prep_emit(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __restrict__ lens,
              const int32_t* __restrict__ owner, const int32_t* __restrict__ ep_pt,
              const int32_t* __restrict__ tp_pt, unsigned int call) {
   DevStatus* st = status_of(g, w);
   if (read_flags(st)) return;
+  const long long nd = (long long)st->ndesc;
   const int lane = threadIdx.x & 31;
-  const int warps_total = (gridDim.x * blockDim.x) >> 5;
-  const int64_t* off = reinterpret_cast<const int64_t*>(g.base + w.req_off);
+  const int64_t* order_start = reinterpret_cast<const int64_t*>(g.base + w.req_off);
+  const int32_t* order_req = reinterpret_cast<const int32_t*>(g.base + w.req_inv);
   umm_kv_desc* desc = reinterpret_cast<umm_kv_desc*>(g.base + w.desc);
   uint32_t* bm = reinterpret_cast<uint32_t*>(g.base + w.bitmap);
   unsigned int oob_any = 0, dup_any = 0;
-  for (int k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < R; k += warps_total) {
-    const int len = lens[k], o = owner[k];
-    const int np = (len + g.ps - 1) / g.ps;
-    const int64_t start = off[k];
-    for (int pb = 0; pb < np; pb += 32) {
-      const int p = pb + lane;
-      bool oob = false, dup = false;
-      if (p < np) {
-        const int ep = ep_pt[(int64_t)k * maxp + p], tp = tp_pt[(int64_t)k * maxp + p];
-        oob = ep < 0 || ep >= g.pages_ep || tp < 0 || tp >= g.pages_tp;
-        if (!oob) {
-          const long long bit = dir == 0 ? (long long)tp : (long long)o * g.pages_ep + ep;
-          const uint32_t m = 1u << (bit & 31);
-          dup = (atomicOr(&bm[bit >> 5], m) & m) != 0;
-        }
-        umm_kv_desc d;
-        d.req = k;
-        d.page = p;
-        d.src_region = dir == 0 ? o : -1;
-        d.dst_region = dir == 0 ? -1 : o;
-        d.src_page = dir == 0 ? ep : tp;
-        d.dst_page = dir == 0 ? tp : ep;
-        d.ntok = min(g.ps, len - p * g.ps);
-        d.reserved = 0;
-        desc[start + p] = d;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  // every lane runs the same number of iterations (the ballots need them all)
+  for (long long base = (long long)blockIdx.x * blockDim.x; base < nd; base += stride) {
+    const long long di = base + threadIdx.x;
+    bool oob = false, dup = false;
+    if (di < nd) {
+      int lo = 0, hi = R - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (order_start[mid] <= di) lo = mid;
+        else hi = mid - 1;
       }
-      oob_any |= __ballot_sync(0xffffffffu, oob);
-      dup_any |= __ballot_sync(0xffffffffu, dup);
+      const int k = order_req[lo];
+      const int p = (int)(di - order_start[lo]);
+      const int len = lens[k], o = owner[k];
+      const int ep = ep_pt[(int64_t)k * maxp + p], tp = tp_pt[(int64_t)k * maxp + p];
+      oob = ep < 0 || ep >= g.pages_ep || tp < 0 || tp >= g.pages_tp;
+      if (!oob) {
+        const long long bit = dir == 0 ? (long long)tp : (long long)o * g.pages_ep + ep;
+        const uint32_t m = 1u << (bit & 31);
+        dup = (atomicOr(&bm[bit >> 5], m) & m) != 0;
+      }
+      umm_kv_desc d;
+      d.req = k;
+      d.page = p;
+      d.src_region = dir == 0 ? o : -1;
+      d.dst_region = dir == 0 ? -1 : o;
+      d.src_page = dir == 0 ? ep : tp;
+      d.dst_page = dir == 0 ? tp : ep;
+      d.ntok = min(g.ps, len - p * g.ps);
+      d.reserved = 0;
+      desc[di] = d;
     }
+    oob_any |= __ballot_sync(0xffffffffu, oob);
+    dup_any |= __ballot_sync(0xffffffffu, dup);
   }
   if (lane == 0) {
     if (__popc(oob_any)) raise_flag(st, UMM_FLAG_PAGE_OOB, call);
@@ -143,9 +173,12 @@ cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (R == 0) return cudaSuccess;
-  int blocks = (R * 32 + 255) / 256;
-  if (blocks > sms * 8) blocks = sms * 8;
-  kv_prep_emit<<<blocks, 256, 0, s>>>(g, w, dir, R, maxp, lens, owner, ep_pt, tp_pt, call);
+  // enough threads for every live page (at most min(capacity, R * maxp))
+  const long long most = std::min<long long>(w.desc_cap, (long long)R * maxp);
+  long long blocks = (most + 255) / 256;
+  if (blocks > (long long)sms * 32) blocks = (long long)sms * 32;
+  if (blocks < 1) blocks = 1;
+  kv_prep_emit<<<(unsigned)blocks, 256, 0, s>>>(g, w, dir, R, maxp, lens, owner, ep_pt, tp_pt, call);
   return cudaGetLastError();
 }
 

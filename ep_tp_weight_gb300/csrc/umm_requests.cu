@@ -82,26 +82,45 @@ static __device__ bool build_inverse(const int32_t* __restrict__ key, int32_t R,
 
 // ------------------------------------------------------------------ placement (TP -> EP)
 
-// Greedy list scheduling with the loads held in registers (PB >= P).
+// Greedy list scheduling over the sorted keys, one thread.  Each rank's load
+// is packed with its index, (load << 6) | q, so one 64-bit minimum yields the
+// least-loaded rank and breaks ties towards the lowest rank.  The choice for
+// sorted position i goes to choice[i] (shared memory): the serial loop touches
+// no global memory.
 template <int PB>
-__device__ void greedy(const unsigned long long* keys, int32_t R, int P, const int32_t* inv,
-                       int32_t* owner) {
-  long long load[PB];
+__device__ void greedy(const unsigned long long* keys, int32_t R, int P, uint8_t* choice) {
+  unsigned long long k[PB];
 #pragma unroll
-  for (int q = 0; q < PB; ++q) load[q] = q < P ? 0 : LLONG_MAX;
+  for (int q = 0; q < PB; ++q) k[q] = q < P ? (unsigned long long)q : ~0ull;
   for (int i = 0; i < R; ++i) {
     const unsigned long long key = keys[i];
-    const int pos = (int)(key & 0xffffffffu);
-    const long long len = 0x7fffffffll - (long long)(key >> 32);
-    int best = 0;
-    long long bl = load[0];
+    const unsigned long long len = 0x7fffffffull - (key >> 32);
+    unsigned long long m[PB];
 #pragma unroll
-    for (int q = 1; q < PB; ++q)
-      if (load[q] < bl) { bl = load[q]; best = q; }   // strict: ties keep the lower rank
+    for (int q = 0; q < PB; ++q) m[q] = k[q];
+#pragma unroll
+    for (int w = PB / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int q = 0; q < w; ++q) m[q] = m[q] < m[q + w] ? m[q] : m[q + w];
+    const int best = (int)(m[0] & 63u);
 #pragma unroll
     for (int q = 0; q < PB; ++q)
-      if (q == best) load[q] += len;
-    owner[inv ? inv[pos] : pos] = best;
+      if (q == best) k[q] += len << 6;
+    choice[i] = (uint8_t)best;
+  }
+}
+
+// The same rule for P > 16, with the packed loads in local memory.
+__device__ __noinline__ void greedy_wide(const unsigned long long* keys, int32_t R, int P, uint8_t* choice) {
+  unsigned long long k[kMaxGroups];
+  for (int q = 0; q < P; ++q) k[q] = (unsigned long long)q;
+  for (int i = 0; i < R; ++i) {
+    const unsigned long long len = 0x7fffffffull - (keys[i] >> 32);
+    unsigned long long m = k[0];
+    for (int q = 1; q < P; ++q) m = k[q] < m ? k[q] : m;
+    const int best = (int)(m & 63u);
+    k[best] += len << 6;
+    choice[i] = (uint8_t)best;
   }
 }
 
@@ -157,12 +176,17 @@ place_kernel(Geo g, Ws w, int32_t R, const int32_t* __restrict__ lens, const int
       __syncthreads();
     }
   }
+  // the rank chosen for sorted position i, then scattered to request order
+  uint8_t* choice = reinterpret_cast<uint8_t*>(g.base + w.choice);
   if (tid == 0) {
-    const int32_t* iv = list_pos ? inv : nullptr;
-    if (P <= 8) greedy<8>(keys, R, P, iv, owner);
-    else if (P <= 16) greedy<16>(keys, R, P, iv, owner);
-    else if (P <= 32) greedy<32>(keys, R, P, iv, owner);
-    else greedy<64>(keys, R, P, iv, owner);
+    if (P <= 8) greedy<8>(keys, R, P, choice);
+    else if (P <= 16) greedy<16>(keys, R, P, choice);
+    else greedy_wide(keys, R, P, choice);
+  }
+  __syncthreads();
+  for (int i = tid; i < R; i += blockDim.x) {
+    const int pos = (int)(keys[i] & 0xffffffffu);
+    owner[list_pos ? inv[pos] : pos] = choice[i];
   }
   __syncthreads();
   // local position = rank among the owner's requests in list order
