@@ -124,7 +124,7 @@ void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
   ws->keys_cap = keys_cap;
   o = align_up(o + (uint64_t)keys_cap * 8, 256);
   ws->choice = o;
-  o = align_up(o + (uint64_t)nreq, 256);
+  o = align_up(o + (uint64_t)nreq + 4, 256);
   ws->bitmap = o;
   ws->bitmap_words = words;
   o = align_up(o + (uint64_t)words * 4, 4096);

@@ -83,44 +83,83 @@ static __device__ bool build_inverse(const int32_t* __restrict__ key, int32_t R,
 // ------------------------------------------------------------------ placement (TP -> EP)
 
 // Greedy list scheduling over the sorted keys, one thread.  Each rank's load
-// is packed with its index, (load << 6) | q, so one 64-bit minimum yields the
-// least-loaded rank and breaks ties towards the lowest rank.  The choice for
-// sorted position i goes to choice[i] (shared memory): the serial loop touches
-// no global memory.
-template <int PB>
-__device__ void greedy(const unsigned long long* keys, int32_t R, int P, uint8_t* choice) {
-  unsigned long long k[PB];
+// is packed with its index, (load << S) | q, so one minimum yields the least
+// loaded rank and breaks ties towards the lowest rank.  With 32-bit words the
+// minimum is a single instruction; 64-bit words are used when the loads might
+// not fit.  The serial loop reads the next key ahead and stores four choices
+// at a time (choice[i] = rank of sorted position i); keys and choices are
+// distinct buffers, so nothing in the loop waits on memory.
+template <typename Word, int PB, int S>
+__device__ void greedy(const unsigned long long* __restrict__ keys, int32_t R, int P,
+                       uint32_t* __restrict__ choice4) {
+  Word k[PB];
 #pragma unroll
-  for (int q = 0; q < PB; ++q) k[q] = q < P ? (unsigned long long)q : ~0ull;
+  for (int q = 0; q < PB; ++q) k[q] = q < P ? (Word)q : (Word)~(Word)0;
+  uint32_t pack = 0;
+  unsigned long long next = R > 0 ? keys[0] : 0ull;
   for (int i = 0; i < R; ++i) {
-    const unsigned long long key = keys[i];
-    const unsigned long long len = 0x7fffffffull - (key >> 32);
-    unsigned long long m[PB];
+    const unsigned long long key = next;
+    if (i + 1 < R) next = keys[i + 1];
+    const Word len = (Word)(0x7fffffffull - (key >> 32));
+    Word m[PB];
 #pragma unroll
     for (int q = 0; q < PB; ++q) m[q] = k[q];
 #pragma unroll
     for (int w = PB / 2; w > 0; w >>= 1)
 #pragma unroll
       for (int q = 0; q < w; ++q) m[q] = m[q] < m[q + w] ? m[q] : m[q + w];
-    const int best = (int)(m[0] & 63u);
+    const int best = (int)(m[0] & (Word)((1u << S) - 1u));
 #pragma unroll
-    for (int q = 0; q < PB; ++q)
-      if (q == best) k[q] += len << 6;
-    choice[i] = (uint8_t)best;
+    for (int q = 0; q < PB; ++q) k[q] += (q == best) ? (len << S) : (Word)0;
+    pack |= (uint32_t)best << (8 * (i & 3));
+    if ((i & 3) == 3 || i + 1 == R) {
+      choice4[i >> 2] = pack;
+      pack = 0;
+    }
   }
 }
 
-// The same rule for P > 16, with the packed loads in local memory.
-__device__ __noinline__ void greedy_wide(const unsigned long long* keys, int32_t R, int P, uint8_t* choice) {
+// The same rule with one rank per lane of a warp (P <= 32, 32-bit packed
+// loads): the least-loaded rank of each step is one warp reduce-min.
+template <int S>
+__device__ void greedy_warp(const unsigned long long* __restrict__ keys, int32_t R, int P,
+                            uint32_t* __restrict__ choice4) {
+  const int lane = threadIdx.x & 31;
+  uint32_t k = lane < P ? (uint32_t)lane : 0xffffffffu;
+  uint32_t pack = 0;
+  unsigned long long next = R > 0 ? keys[0] : 0ull;
+  for (int i = 0; i < R; ++i) {
+    const unsigned long long key = next;
+    if (i + 1 < R) next = keys[i + 1];
+    const uint32_t len = (uint32_t)(0x7fffffffull - (key >> 32));
+    const uint32_t m = __reduce_min_sync(0xffffffffu, k);
+    const int best = (int)(m & ((1u << S) - 1u));
+    if (lane == best) k += len << S;
+    pack |= (uint32_t)best << (8 * (i & 3));
+    if ((i & 3) == 3 || i + 1 == R) {
+      if (lane == 0) choice4[i >> 2] = pack;
+      pack = 0;
+    }
+  }
+}
+
+// The same rule for P > 16, with the loads in local memory.
+__device__ __noinline__ void greedy_wide(const unsigned long long* __restrict__ keys, int32_t R, int P,
+                                         uint32_t* __restrict__ choice4) {
   unsigned long long k[kMaxGroups];
   for (int q = 0; q < P; ++q) k[q] = (unsigned long long)q;
+  uint32_t pack = 0;
   for (int i = 0; i < R; ++i) {
     const unsigned long long len = 0x7fffffffull - (keys[i] >> 32);
     unsigned long long m = k[0];
     for (int q = 1; q < P; ++q) m = k[q] < m ? k[q] : m;
     const int best = (int)(m & 63u);
     k[best] += len << 6;
-    choice[i] = (uint8_t)best;
+    pack |= (uint32_t)best << (8 * (i & 3));
+    if ((i & 3) == 3 || i + 1 == R) {
+      choice4[i >> 2] = pack;
+      pack = 0;
+    }
   }
 }
 
@@ -134,13 +173,24 @@ place_kernel(Geo g, Ws w, int32_t R, const int32_t* __restrict__ lens, const int
   __shared__ long long carry[kMaxGroups];
   __shared__ long long warp_tot[32 * kMaxGroups];
   __shared__ int bad;
+  __shared__ unsigned long long total_len_s;
   const int tid = threadIdx.x, P = g.P;
-  if (tid == 0) bad = 0;
+  if (tid == 0) {
+    bad = 0;
+    total_len_s = 0;
+  }
   if (tid < kMaxGroups) carry[tid] = 0;
   __syncthreads();
-  for (int k = tid; k < R; k += blockDim.x)
+  unsigned long long my_len = 0;
+  for (int k = tid; k < R; k += blockDim.x) {
     if (lens[k] < 0) bad = 1;
+    else my_len += (unsigned long long)lens[k];
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) my_len += __shfl_xor_sync(0xffffffffu, my_len, d);
+  if ((tid & 31) == 0) atomicAdd(&total_len_s, my_len);
   __syncthreads();
+  const unsigned long long total_len = total_len_s;
   int32_t* inv = reinterpret_cast<int32_t*>(g.base + w.req_inv);
   bool ok = bad == 0;
   if (ok && list_pos) ok = build_inverse(list_pos, R, inv, &bad);
@@ -176,12 +226,18 @@ place_kernel(Geo g, Ws w, int32_t R, const int32_t* __restrict__ lens, const int
       __syncthreads();
     }
   }
-  // the rank chosen for sorted position i, then scattered to request order
+  // the rank chosen for sorted position i, then scattered to request order;
+  // 32-bit packed loads when the total of all lengths, shifted, fits
   uint8_t* choice = reinterpret_cast<uint8_t*>(g.base + w.choice);
-  if (tid == 0) {
-    if (P <= 8) greedy<8>(keys, R, P, choice);
-    else if (P <= 16) greedy<16>(keys, R, P, choice);
-    else greedy_wide(keys, R, P, choice);
+  uint32_t* c4 = reinterpret_cast<uint32_t*>(choice);
+  if (tid < 32 && P <= 8 && total_len < (1ull << 29)) {
+    greedy_warp<3>(keys, R, P, c4);
+  } else if (tid < 32 && P <= 32 && total_len < (1ull << 27)) {
+    greedy_warp<5>(keys, R, P, c4);
+  } else if (tid == 0) {
+    if (P <= 8) greedy<unsigned long long, 8, 6>(keys, R, P, c4);
+    else if (P <= 16) greedy<unsigned long long, 16, 6>(keys, R, P, c4);
+    else greedy_wide(keys, R, P, c4);
   }
   __syncthreads();
   for (int i = tid; i < R; i += blockDim.x) {
