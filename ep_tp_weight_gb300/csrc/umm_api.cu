@@ -127,7 +127,11 @@ void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
   o = align_up(o + (uint64_t)nreq + 4, 256);
   ws->bitmap = o;
   ws->bitmap_words = words;
-  o = align_up(o + (uint64_t)words * 4, 4096);
+  o = align_up(o + (uint64_t)words * 4, 256);
+  ws->tp_bitmap = o;
+  o = align_up(o + (uint64_t)((L->pages_tp + 31) / 32 + 1) * 4, 256);
+  ws->sched = o;
+  o = align_up(o + (uint64_t)L->pages_tp * 8, 4096);
   ws->max_requests = (int32_t)nreq;
   L->ws_bytes = o - L->ws_off;
   L->total_bytes = o;
@@ -183,19 +187,23 @@ int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, co
   if (u->kv_mode != from) return UMM_ERR_MODE;
   cudaStream_t s = as_stream(stream);
   const unsigned int call = new_call(u);
+  // live pages <= min(descriptor capacity, R * pages per request).  When they
+  // may fill half the TP pool or more, the copies walk the pool in TP-page
+  // order (measured on GB300: +1.7% EP->TP, +2.3% TP->EP over list order).
+  const int64_t max_desc = std::min<int64_t>(u->ws.desc_cap, (int64_t)R * maxp);
+  const int use_sched = max_desc > 0 && 2 * max_desc >= u->L.pages_tp;
   {
     ProfScope ps(u, UMM_K_KV_PREP, s);
-    rc = cuda_rc(uk::launch_kv_prep(u->geo, u->ws, dir, R, maxp, lens, owner, ep_pt, tp_pt, call, s, u->sms));
+    rc = cuda_rc(uk::launch_kv_prep(u->geo, u->ws, dir, R, maxp, lens, owner, ep_pt, tp_pt, call, use_sched, s,
+                                    u->sms));
   }
   if (rc) return rc;
   u->launches += R > 0 ? 2 : 1;
   const int N = u->dims.num_layers;
-  // live pages <= min(descriptor capacity, R * pages per request): the grid
-  const int64_t max_desc = std::min<int64_t>(u->ws.desc_cap, (int64_t)R * maxp);
   for (int t = 0; t < N; ++t) {
     const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
     ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
-    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, s));
+    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s));
     if (rc) return rc;
     if (max_desc > 0) ++u->launches;
   }
@@ -297,7 +305,9 @@ int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) 
   g.h_tp = u->L.h_tp;
   u->weight_mode = dims->weight_mode;
   u->kv_mode = dims->kv_mode;
+  // status block and TP-page schedule start at zero (call id 0 is never used)
   if (cudaMemset(g.base + u->ws.status, 0, kStatusBytes) != cudaSuccess ||
+      (u->L.pages_tp > 0 && cudaMemset(g.base + u->ws.sched, 0, (size_t)u->L.pages_tp * 8) != cudaSuccess) ||
       cudaDeviceSynchronize() != cudaSuccess) {
     delete u;
     return UMM_ERR_CUDA;

@@ -84,17 +84,23 @@ struct Ws {
   uint64_t choice;     // uint8[max_requests]   placement: rank per sorted position
   uint64_t bitmap;     // uint32[bitmap_words]  destination-page use bits
   int64_t bitmap_words;
+  uint64_t tp_bitmap;  // uint32[(pages_tp+31)/32] TP source pages read by TP->EP
+  uint64_t sched;      // uint64[pages_tp]      TP page -> (call << 32 | descriptor)
   int32_t max_requests;
 };
 
 // ---- launchers (enqueue only; all arguments already validated) ----
 cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s);
 
+// use_sched: also index the descriptors by TP page (see launch_kv_copy).
 cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_t maxp,
                            const int32_t* lens, const int32_t* owner, const int32_t* ep_pt,
-                           const int32_t* tp_pt, unsigned int call, cudaStream_t s, int sms);
-// max_desc: an upper bound on the descriptors of the call (the grid size).
-cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, cudaStream_t s);
+                           const int32_t* tp_pt, unsigned int call, int use_sched, cudaStream_t s, int sms);
+// max_desc: an upper bound on the descriptors of the call.  With use_sched
+// the grid walks the TP page pool (descriptors in TP-page order, empty pages
+// exit at once); otherwise it walks the descriptor list.
+cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
+                           unsigned int call, cudaStream_t s);
 
 cudaError_t launch_order(const Geo& g, const Ws& w, int32_t R, const int32_t* owner, int32_t* tp_pos,
                          unsigned int call, cudaStream_t s);

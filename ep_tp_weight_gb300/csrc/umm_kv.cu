@@ -101,11 +101,15 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
       order_req[j] = k;
     }
   }
-  // clear the destination-page bitmap
+  // clear the destination-page bitmap (and, for TP->EP, the TP source one)
   const long long bits = dir == 0 ? g.pages_tp : (long long)P * g.pages_ep;
   const long long words = (bits + 31) / 32;
   uint32_t* bm = reinterpret_cast<uint32_t*>(g.base + w.bitmap);
   for (long long i = tid; i < words; i += blockDim.x) bm[i] = 0u;
+  if (dir == 1) {
+    uint32_t* tb = reinterpret_cast<uint32_t*>(g.base + w.tp_bitmap);
+    for (long long i = tid; i < (g.pages_tp + 31) / 32; i += blockDim.x) tb[i] = 0u;
+  }
 }
 
 // One thread per descriptor: a binary search over the request order finds
@@ -114,7 +118,7 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
 __global__ void __launch_bounds__(256)
 kv_prep_emit(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __restrict__ lens,
              const int32_t* __restrict__ owner, const int32_t* __restrict__ ep_pt,
-             const int32_t* __restrict__ tp_pt, unsigned int call) {
+             const int32_t* __restrict__ tp_pt, unsigned int call, int use_sched) {
   DevStatus* st = status_of(g, w);
   if (read_flags(st)) return;
   const long long nd = (long long)st->ndesc;
@@ -123,6 +127,8 @@ kv_prep_emit(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
   const int32_t* order_req = reinterpret_cast<const int32_t*>(g.base + w.req_inv);
   umm_kv_desc* desc = reinterpret_cast<umm_kv_desc*>(g.base + w.desc);
   uint32_t* bm = reinterpret_cast<uint32_t*>(g.base + w.bitmap);
+  uint32_t* tb = reinterpret_cast<uint32_t*>(g.base + w.tp_bitmap);
+  unsigned long long* sched = reinterpret_cast<unsigned long long*>(g.base + w.sched);
   unsigned int oob_any = 0, dup_any = 0;
   const long long stride = (long long)gridDim.x * blockDim.x;
   // every lane runs the same number of iterations (the ballots need them all)
@@ -145,6 +151,11 @@ kv_prep_emit(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
         const long long bit = dir == 0 ? (long long)tp : (long long)o * g.pages_ep + ep;
         const uint32_t m = 1u << (bit & 31);
         dup = (atomicOr(&bm[bit >> 5], m) & m) != 0;
+        if (dir == 1) {   // each TP page belongs to one request
+          const uint32_t mt = 1u << (tp & 31);
+          dup |= (atomicOr(&tb[tp >> 5], mt) & mt) != 0;
+        }
+        if (use_sched) sched[tp] = ((unsigned long long)call << 32) | (unsigned long long)di;
       }
       umm_kv_desc d;
       d.req = k;
@@ -168,7 +179,7 @@ kv_prep_emit(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
 
 cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_t maxp,
                            const int32_t* lens, const int32_t* owner, const int32_t* ep_pt,
-                           const int32_t* tp_pt, unsigned int call, cudaStream_t s, int sms) {
+                           const int32_t* tp_pt, unsigned int call, int use_sched, cudaStream_t s, int sms) {
   kv_prep_scan<<<1, kScanThreads, 0, s>>>(g, w, dir, R, maxp, lens, owner, call);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -178,7 +189,7 @@ cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_
   long long blocks = (most + 255) / 256;
   if (blocks > (long long)sms * 32) blocks = (long long)sms * 32;
   if (blocks < 1) blocks = 1;
-  kv_prep_emit<<<(unsigned)blocks, 256, 0, s>>>(g, w, dir, R, maxp, lens, owner, ep_pt, tp_pt, call);
+  kv_prep_emit<<<(unsigned)blocks, 256, 0, s>>>(g, w, dir, R, maxp, lens, owner, ep_pt, tp_pt, call, use_sched);
   return cudaGetLastError();
 }
 
@@ -188,14 +199,32 @@ struct KVParams {
   uint8_t* base;
   const umm_kv_desc* desc;
   const DevStatus* st;
+  const unsigned long long* sched;   // TP page -> (call << 32 | descriptor), or null
+  unsigned int call;
   uint64_t region_stride, kv_v_off;
   uint64_t ep_slot, tp_slot;   // absolute offsets of the slot inside a region
   uint64_t ep_row, tp_row;     // bytes per token row: Hkv*D*2, h_tp*D*2
   uint64_t head_bytes;         // D*2
   uint32_t ps, Hkv, P, h_tp, rep;   // rep = ranks per head when Hkv < P (else 1)
   uint32_t half_vec;           // vectors in one half (K or V) of an EP page
+  long long pages_tp;
   FastDiv half, tok, dv;       // divisors: half_vec, Hkv*Dv, Dv
 };
+
+// The descriptor a CTA works on for grid position di: in TP-page order
+// through the schedule (false for pages this call does not use), or straight
+// from the descriptor list.
+__device__ __forceinline__ bool fetch_desc(const KVParams& p, unsigned long long di, umm_kv_desc& d) {
+  if (p.sched) {
+    const unsigned long long e = p.sched[di];
+    const unsigned long long idx = e & 0xffffffffull;
+    if ((unsigned int)(e >> 32) != p.call || idx >= p.st->ndesc) return false;
+    d = p.desc[idx];
+    return true;
+  }
+  d = p.desc[di];
+  return true;
+}
 
 // EP -> TP: each source vector of an EP page is loaded once and stored to
 // every TP rank holding its head (rank h*rep + j, local head 0, when Hkv < P;
@@ -204,10 +233,11 @@ template <int VB, int U, int T>
 __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
   using V = typename VecT<VB>::T;
   if (read_flags(p.st)) return;
-  const unsigned long long nd = p.st->ndesc;
+  const unsigned long long nd = p.sched ? (unsigned long long)p.pages_tp : p.st->ndesc;
   const uint32_t nvec = 2 * p.half_vec;
   for (unsigned long long di = blockIdx.x; di < nd; di += gridDim.x) {
-    const umm_kv_desc d = p.desc[di];
+    umm_kv_desc d;
+    if (!fetch_desc(p, di, d)) continue;
     uint8_t* const src_region = p.base + (uint64_t)d.src_region * p.region_stride + p.ep_slot;
     const uint64_t src_page = (uint64_t)d.src_page * p.ps * p.ep_row;
     const uint64_t dst_page = (uint64_t)d.dst_page * p.ps * p.tp_row;
@@ -254,10 +284,11 @@ template <int VB, int U, int T>
 __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
   using V = typename VecT<VB>::T;
   if (read_flags(p.st)) return;
-  const unsigned long long nd = p.st->ndesc;
+  const unsigned long long nd = p.sched ? (unsigned long long)p.pages_tp : p.st->ndesc;
   const uint32_t nvec = 2 * p.half_vec;
   for (unsigned long long di = blockIdx.x; di < nd; di += gridDim.x) {
-    const umm_kv_desc d = p.desc[di];
+    umm_kv_desc d;
+    if (!fetch_desc(p, di, d)) continue;
     uint8_t* const dst_region = p.base + (uint64_t)d.dst_region * p.region_stride + p.ep_slot;
     const uint64_t dst_page = (uint64_t)d.dst_page * p.ps * p.ep_row;
     const uint64_t src_page = (uint64_t)d.src_page * p.ps * p.tp_row;
@@ -319,7 +350,8 @@ cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t 
 }
 }  // namespace
 
-cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, cudaStream_t s) {
+cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
+                           unsigned int call, cudaStream_t s) {
   int VB = 2;
   if (g.D % 8 == 0) VB = 16;
   else if (g.D % 4 == 0) VB = 8;
@@ -330,6 +362,10 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.base = g.base;
   p.desc = reinterpret_cast<const umm_kv_desc*>(g.base + w.desc);
   p.st = reinterpret_cast<const DevStatus*>(g.base + w.status);
+  p.sched = use_sched ? reinterpret_cast<const unsigned long long*>(g.base + w.sched) : nullptr;
+  p.call = call;
+  p.pages_tp = g.pages_tp;
+  if (use_sched) max_desc = g.pages_tp;   // one CTA per TP page
   p.region_stride = g.region_stride;
   p.kv_v_off = g.kv_v_off;
   p.ep_slot = g.kvslots_off + (uint64_t)(layer + 1) * g.kvslot_stride;

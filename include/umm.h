@@ -148,8 +148,9 @@ int umm_layout_for_dims(const umm_dims* dims, umm_layout_t* out);
 
 /* Bind a handle to a caller-owned device buffer of at least
  * umm_required_bytes() bytes, base 256-byte aligned (§4.2: the one
- * allocation, made once at start-up).  Initialises the workspace status block
- * (synchronous memset); everything else in the buffer is left as is.
+ * allocation, made once at start-up).  Initialises the workspace's status
+ * block and TP-page schedule (synchronous memsets); everything else in the
+ * buffer is left as is.
  * Errors: INVALID_ARG, ALIGN, CAPACITY (bytes too small), CUDA. */
 int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out);
 

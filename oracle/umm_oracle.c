@@ -307,9 +307,13 @@ uint32_t orc_kv_validate(const int64_t *d, int dir, int64_t R, int64_t maxp,
       if (per_region[r] > pages_ep) flags |= ORC_F_CAPACITY;
   free(per_region);
   if (flags) return flags;
-  /* page ids in range, destinations used at most once */
+  /* page ids in range; destinations used at most once; and, since a page
+   * holds the tokens of one request only (§3.2 page tables; no prefix sharing
+   * in the setting of §6.1), the TP pages a TP->EP switch reads are distinct
+   * too */
   int64_t dst_pool = (dir == 0) ? pages_tp : P * pages_ep;
   uint8_t *used = calloc((size_t)(dst_pool > 0 ? dst_pool : 1), 1);
+  uint8_t *tp_used = calloc((size_t)(pages_tp > 0 ? pages_tp : 1), 1);
   for (int64_t k = 0; k < R; ++k) {
     int64_t np = npages_of(lens[k], ps);
     for (int64_t p = 0; p < np; ++p) {
@@ -321,8 +325,13 @@ uint32_t orc_kv_validate(const int64_t *d, int dir, int64_t R, int64_t maxp,
       int64_t slot = (dir == 0) ? tp : owner[k] * pages_ep + ep;
       if (used[slot]) flags |= ORC_F_DUP_PAGE;
       used[slot] = 1;
+      if (dir == 1) {
+        if (tp_used[tp]) flags |= ORC_F_DUP_PAGE;
+        tp_used[tp] = 1;
+      }
     }
   }
+  free(tp_used);
   free(used);
   return flags;
 }

@@ -34,6 +34,9 @@ KV_CASES = [
     Workload("kv_hkv1_p4_d5", P=4, N=2, Hkv=1, D=5, ps=3, R=7, len_a=1, len_b=20),
     Workload("kv_hkv4_p8_d128", P=8, N=2, Hkv=4, D=128, ps=16, R=40, len_a=1, len_b=300, kv_sigma=1.0),
     Workload("kv_hkv4_p4_many_pages", P=4, N=2, Hkv=4, D=16, ps=8, R=300, len_a=1, len_b=200),
+    # a pool much larger than the live pages: the copies walk the descriptor
+    # list instead of the TP page pool
+    Workload("kv_sparse_pool", P=4, N=2, Hkv=2, D=8, ps=4, R=9, len_a=1, len_b=23, slack=8.0),
 ]
 
 
@@ -201,6 +204,19 @@ def test_kv_device_errors_leave_buffer_untouched():
         assert (code_got, flags) == (code, want), name
         assert umm.umm_get_modes(dev.h)[1] == umm.UMM_MODE_EP      # ... restored by the sync
         np.testing.assert_array_equal(dev.host(), ref)
+    # TP -> EP: two requests reading the same TP page
+    umm.umm_set_modes(dev.h, umm.UMM_MODE_EP, umm.UMM_MODE_TP)
+    owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+    free2 = synth.permutation(8, 4, L["pages_ep"], rows=d.P)
+    _, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, maxp, free2, region=owner2, key=st.tp_pos)
+    bad_tp = st.tp_pt.copy()
+    bad_tp[k2, 1] = bad_tp[0, 0]
+    want = oracle.kv_validate(d, 1, st.lens, owner2, ep_pt2, bad_tp)
+    umm.reshard_kv_tp2ep(dev.h, len(st.lens), maxp, i32(st.lens), i32(owner2), i32(ep_pt2), i32(bad_tp))
+    assert dev.status() == (umm.UMM_ERR_DUP_PAGE, want) and want == oracle.F_DUP_PAGE
+    assert umm.umm_get_modes(dev.h)[1] == umm.UMM_MODE_TP
+    np.testing.assert_array_equal(dev.host(), ref)
+    umm.umm_set_modes(dev.h, umm.UMM_MODE_EP, umm.UMM_MODE_EP)
     # sticky: a failed page hand-out stops the following KV call too
     big = np.full(len(st.lens), 10**6, np.int32)
     pt = torch.zeros(st.tp_pt.shape, dtype=torch.int32, device="cuda")

@@ -463,6 +463,14 @@ def test_kv_validation_flags():
     small = dims_of(w, pages_tp=int(synth.npages(st.lens, d.ps).sum()) - 2)
     assert oracle.kv_validate(small, 0, st.lens, st.owner, st.ep_pt, np.zeros_like(st.tp_pt)) \
         & oracle.F_CAPACITY
+    # TP -> EP: two requests claiming the same TP page
+    owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+    free2 = synth.permutation(8, 4, L["pages_ep"], rows=d.P)
+    _, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, st.ep_pt.shape[1], free2, region=owner2, key=st.tp_pos)
+    assert oracle.kv_validate(d, 1, st.lens, owner2, ep_pt2, st.tp_pt) == 0
+    bad_tp = st.tp_pt.copy()
+    bad_tp[k2, 1] = bad_tp[0, 0]
+    assert oracle.kv_validate(d, 1, st.lens, owner2, ep_pt2, bad_tp) == oracle.F_DUP_PAGE
     # TP -> EP: one EP rank asked to hold more than its pool
     many = np.zeros_like(st.owner)
     fl = oracle.kv_validate(d, 1, st.lens, many, st.ep_pt, st.tp_pt)
