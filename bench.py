@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-staged", action="store_true")
     return ap.parse_args()
 
 
@@ -371,6 +372,66 @@ def run_umm(args, rank, world, local_rank):
                  "unit": UNIT, "steps": 2 * reps}
         del g
 
+    # ---------------- the staged (collective-style) path, same steps, for comparison
+    staged = None
+    if not args.no_staged:
+        wsb = umm.umm_weights_stage_bytes(h) if w.E else 0
+        ksb = umm.umm_kv_stage_bytes(h) if have_kv else 0
+        wsb_al = (wsb + 255) // 256 * 256
+        stage_buf = torch.empty(wsb_al + ksb, dtype=torch.uint8, device=dev)
+        w_stage, k_stage = stage_buf.data_ptr(), stage_buf.data_ptr() + wsb_al
+
+        def step_staged():
+            if w.E:
+                umm.reshard_weights_ep2tp_staged(h, w_stage, wsb, s)
+            if have_kv:
+                umm.gather_requests_ep2tp(h, R, state["owner"], tp_pos, s)
+                umm.umm_assign_pages(h, 1, R, lens, None, tp_pos, tp_free, L["pages_tp"], L["pages_tp"], tp_pt,
+                                     maxp, s)
+                umm.reshard_kv_ep2tp_staged(h, k_stage, ksb, R, maxp, lens, state["owner"], state["ep_pt"], tp_pt, s)
+                umm.place_requests_tp2ep(h, R, lens, tp_pos, state["owner_n"], local, s)
+                umm.umm_assign_pages(h, P, R, lens, state["owner_n"], tp_pos, ep_free, L["pages_ep"],
+                                     L["pages_ep"], state["ep_pt_n"], maxp, s)
+            if w.E:
+                umm.reshard_weights_tp2ep_staged(h, w_stage, wsb, s)
+            if have_kv:
+                umm.reshard_kv_tp2ep_staged(h, k_stage, ksb, R, maxp, lens, state["owner_n"], state["ep_pt_n"],
+                                            tp_pt, s)
+                state["owner"], state["owner_n"] = state["owner_n"], state["owner"]
+                state["ep_pt"], state["ep_pt_n"] = state["ep_pt_n"], state["ep_pt"]
+
+        step_staged()                                   # warm-up
+        torch.cuda.synchronize()
+        umm.umm_profile_enable(h, True)
+        umm.umm_profile_reset(h)
+        reps = max(2, args.steps // 2)
+        barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(s)
+        for _ in range(reps):
+            step_staged()
+        s1.record(s)
+        torch.cuda.synchronize()
+        ms_s = max_over_ranks(s0.elapsed_time(s1), dev) / reps
+        sprof = {umm.KIND_NAMES[k]: umm.umm_profile_read(h, k) for k in range(umm.K_COUNT)}
+        umm.umm_profile_enable(h, False)
+        code, _ = umm.umm_status_sync(h, s)
+        if code:
+            raise RuntimeError(f"staged steps failed: {umm.strerror(code)}")
+        staged = {"ms_per_step": round(ms_s, 3),
+                  "value": round(whole_job_gbs(bytes_model["step"], 1, ms_s, world), 1), "unit": UNIT,
+                  "steps": reps, "stage_bytes": int(wsb_al + ksb)}
+        if w.E and sprof["weights_ep2tp"][0]:
+            staged["weights_ms_per_layer"] = round(
+                (sprof["weights_ep2tp"][1] + sprof["weights_tp2ep"][1]) /
+                (sprof["weights_ep2tp"][0] + sprof["weights_tp2ep"][0]), 4)
+        if have_kv and sprof["kv_ep2tp"][0]:
+            staged["kv_ep2tp_ms_per_switch"] = round(sprof["kv_ep2tp"][1] / sprof["kv_ep2tp"][0], 3)
+            staged["kv_tp2ep_ms_per_switch"] = round(sprof["kv_tp2ep"][1] / sprof["kv_tp2ep"][0], 3)
+        del stage_buf
+        torch.cuda.empty_cache()
+
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and have_kv:
@@ -413,7 +474,7 @@ def run_umm(args, rank, world, local_rank):
     umm.umm_destroy(h)
     del buf
     torch.cuda.empty_cache()
-    return dict(w=w, lens=lens_h, ms_total=ms_total, graph=graph, launches=launches, prof=prof, clocks=clk.summary(),
+    return dict(w=w, lens=lens_h, ms_total=ms_total, graph=graph, staged=staged, launches=launches, prof=prof, clocks=clk.summary(),
                 ms_ep2tp=ms_ep2tp, ms_tp2ep=ms_tp2ep, bytes=bytes_model, e2e=e2e, layout=L, nbytes=nbytes)
 
 
@@ -588,6 +649,8 @@ def main():
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": per_launch_bytes},
         "cuda_graph": r["graph"],
+        "staged_comparison": None if r["staged"] is None else dict(
+            r["staged"], fused_speedup=round(r["staged"]["ms_per_step"] / ms_step, 3)),
         "clocks": r["clocks"], "gpu_launches": r["launches"],
         "e2e": r["e2e"],
     }

@@ -100,6 +100,12 @@ _SIG = {
     "umm_profile_reset": [_vp],
     "umm_launch_count": [_vp, _P(_i64)],
     "place_requests_tp2ep_noalloc": [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "umm_weights_stage_bytes": [_vp, _P(_u64)],
+    "reshard_weights_ep2tp_staged": [_vp, _vp, _u64, _vp],
+    "reshard_weights_tp2ep_staged": [_vp, _vp, _u64, _vp],
+    "umm_kv_stage_bytes": [_vp, _P(_u64)],
+    "reshard_kv_ep2tp_staged": [_vp, _vp, _u64, _i32, _i32, _vp, _vp, _vp, _vp, _vp],
+    "reshard_kv_tp2ep_staged": [_vp, _vp, _u64, _i32, _i32, _vp, _vp, _vp, _vp, _vp],
     "umm_policy_create": [_vp, _P(_vp)],
     "umm_policy_destroy": [_vp],
     "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
@@ -192,6 +198,42 @@ def reshard_weights_ep2tp(h: int, stream=None) -> None:
 
 def reshard_weights_tp2ep(h: int, stream=None) -> None:
     _ck(_lib.reshard_weights_tp2ep(h, _stream(stream)), "reshard_weights_tp2ep")
+
+
+def umm_weights_stage_bytes(h: int) -> int:
+    out = ctypes.c_uint64()
+    _ck(_lib.umm_weights_stage_bytes(h, ctypes.byref(out)), "umm_weights_stage_bytes")
+    return out.value
+
+
+def reshard_weights_ep2tp_staged(h: int, stage, stage_bytes: int, stream=None) -> None:
+    _ck(_lib.reshard_weights_ep2tp_staged(h, _ptr(stage), int(stage_bytes), _stream(stream)),
+        "reshard_weights_ep2tp_staged")
+
+
+def reshard_weights_tp2ep_staged(h: int, stage, stage_bytes: int, stream=None) -> None:
+    _ck(_lib.reshard_weights_tp2ep_staged(h, _ptr(stage), int(stage_bytes), _stream(stream)),
+        "reshard_weights_tp2ep_staged")
+
+
+def umm_kv_stage_bytes(h: int) -> int:
+    out = ctypes.c_uint64()
+    _ck(_lib.umm_kv_stage_bytes(h, ctypes.byref(out)), "umm_kv_stage_bytes")
+    return out.value
+
+
+def reshard_kv_ep2tp_staged(h: int, stage, stage_bytes: int, R: int, max_pages_per_req: int, seq_lens,
+                            ep_owner, ep_page_table, tp_page_table, stream=None) -> None:
+    _ck(_lib.reshard_kv_ep2tp_staged(h, _ptr(stage), int(stage_bytes), R, max_pages_per_req, _ptr(seq_lens),
+                                     _ptr(ep_owner), _ptr(ep_page_table), _ptr(tp_page_table), _stream(stream)),
+        "reshard_kv_ep2tp_staged")
+
+
+def reshard_kv_tp2ep_staged(h: int, stage, stage_bytes: int, R: int, max_pages_per_req: int, seq_lens,
+                            ep_owner, ep_page_table, tp_page_table, stream=None) -> None:
+    _ck(_lib.reshard_kv_tp2ep_staged(h, _ptr(stage), int(stage_bytes), R, max_pages_per_req, _ptr(seq_lens),
+                                     _ptr(ep_owner), _ptr(ep_page_table), _ptr(tp_page_table), _stream(stream)),
+        "reshard_kv_tp2ep_staged")
 
 
 def gather_requests_ep2tp(h: int, R: int, ep_owner, tp_pos, stream=None) -> None:

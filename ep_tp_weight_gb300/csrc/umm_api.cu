@@ -131,7 +131,11 @@ void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
   ws->tp_bitmap = o;
   o = align_up(o + (uint64_t)((L->pages_tp + 31) / 32 + 1) * 4, 256);
   ws->sched = o;
-  o = align_up(o + (uint64_t)L->pages_tp * 8, 4096);
+  o = align_up(o + (uint64_t)L->pages_tp * 8, 256);
+  ws->order_tok = o;
+  o = align_up(o + (uint64_t)nreq * 8, 256);
+  ws->rank_info = o;
+  o = align_up(o + (uint64_t)3 * uk::kMaxGroups * 8, 4096);
   ws->max_requests = (int32_t)nreq;
   L->ws_bytes = o - L->ws_off;
   L->total_bytes = o;
@@ -224,6 +228,58 @@ int reshard_weights(umm* u, int ep2tp, void* stream) {
     int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s));
     if (rc) return rc;
     ++u->launches;
+  }
+  u->weight_mode = ep2tp ? UMM_MODE_TP : UMM_MODE_EP;
+  return UMM_OK;
+}
+
+int reshard_kv_staged(umm* u, int dir, void* d_stage, uint64_t stage_bytes, int32_t R, int32_t maxp,
+                      const int32_t* lens, const int32_t* owner, const int32_t* ep_pt, const int32_t* tp_pt,
+                      void* stream) {
+  int rc = check_kv_args(u, R, maxp, lens, owner, ep_pt, tp_pt);
+  if (rc) return rc;
+  if (!d_stage) return UMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_stage) % 256) return UMM_ERR_ALIGN;
+  if (stage_bytes < uk::kv_stage_bytes(u->geo)) return UMM_ERR_CAPACITY;
+  if (u->kv_mode != (dir == 0 ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
+  cudaStream_t s = as_stream(stream);
+  const unsigned int call = new_call(u);
+  {
+    ProfScope ps(u, UMM_K_KV_PREP, s);
+    rc = cuda_rc(uk::launch_kv_prep(u->geo, u->ws, dir, R, maxp, lens, owner, ep_pt, tp_pt, call, 0, s, u->sms));
+  }
+  if (rc) return rc;
+  u->launches += R > 0 ? 2 : 1;
+  {
+    ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
+    int n = 0;
+    rc = cuda_rc(uk::launch_kv_staged(u->geo, u->ws, dir, R, lens, owner, static_cast<uint8_t*>(d_stage),
+                                      reinterpret_cast<int64_t*>(u->geo.base + u->ws.order_tok),
+                                      reinterpret_cast<int64_t*>(u->geo.base + u->ws.rank_info), call, s, u->sms,
+                                      &n));
+    u->launches += n;
+  }
+  if (rc) return rc;
+  u->kv_log.push_back(KvCall{call, u->kv_mode});
+  if (u->kv_log.size() > 4096) u->kv_log.erase(u->kv_log.begin());
+  u->kv_mode = dir == 0 ? UMM_MODE_TP : UMM_MODE_EP;
+  return UMM_OK;
+}
+
+int reshard_weights_staged(umm* u, int ep2tp, void* d_stage, uint64_t stage_bytes, void* stream) {
+  if (!u || u->dims.E == 0 || !d_stage) return UMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_stage) % 256) return UMM_ERR_ALIGN;
+  if (stage_bytes < uk::weights_stage_bytes(u->geo)) return UMM_ERR_CAPACITY;
+  if (u->weight_mode != (ep2tp ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
+  cudaStream_t s = as_stream(stream);
+  const int N = u->dims.num_layers;
+  for (int t = 0; t < N; ++t) {
+    const int layer = ep2tp ? t : N - 1 - t;
+    ProfScope ps(u, ep2tp ? UMM_K_WEIGHTS_EP2TP : UMM_K_WEIGHTS_TP2EP, s);
+    int n = 0;
+    int rc = cuda_rc(uk::launch_weights_staged(u->geo, ep2tp, layer, static_cast<uint8_t*>(d_stage), s, &n));
+    if (rc) return rc;
+    u->launches += n;
   }
   u->weight_mode = ep2tp ? UMM_MODE_TP : UMM_MODE_EP;
   return UMM_OK;
@@ -354,6 +410,20 @@ int umm_set_modes(umm_t* u, int32_t weight_mode, int32_t kv_mode) {
 int reshard_weights_ep2tp(umm_t* u, void* stream) { return reshard_weights(u, 1, stream); }
 int reshard_weights_tp2ep(umm_t* u, void* stream) { return reshard_weights(u, 0, stream); }
 
+int umm_weights_stage_bytes(const umm_t* u, uint64_t* bytes_out) {
+  if (!u || !bytes_out || u->dims.E == 0) return UMM_ERR_INVALID_ARG;
+  *bytes_out = uk::weights_stage_bytes(u->geo);
+  return UMM_OK;
+}
+
+int reshard_weights_ep2tp_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, void* stream) {
+  return reshard_weights_staged(u, 1, d_stage, stage_bytes, stream);
+}
+
+int reshard_weights_tp2ep_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, void* stream) {
+  return reshard_weights_staged(u, 0, d_stage, stage_bytes, stream);
+}
+
 int gather_requests_ep2tp(umm_t* u, int32_t R, const int32_t* d_ep_owner, int32_t* d_tp_pos, void* stream) {
   if (!u || R < 0 || R > u->ws.max_requests) return UMM_ERR_INVALID_ARG;
   if (R > 0 && (!d_ep_owner || !d_tp_pos)) return UMM_ERR_INVALID_ARG;
@@ -395,6 +465,26 @@ int umm_assign_pages(umm_t* u, int32_t npools, int32_t R, const int32_t* d_seq_l
   u->launches += 2;
   return cuda_rc(uk::launch_assign(u->geo, u->ws, npools, R, d_seq_lens, d_pool, d_key, d_free_pages,
                                    free_stride, free_count, d_page_table, max_pages_per_req, call, s, u->sms));
+}
+
+int umm_kv_stage_bytes(const umm_t* u, uint64_t* bytes_out) {
+  if (!u || !bytes_out || u->dims.num_kv_heads == 0) return UMM_ERR_INVALID_ARG;
+  *bytes_out = uk::kv_stage_bytes(u->geo);
+  return UMM_OK;
+}
+
+int reshard_kv_ep2tp_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, int32_t R, int32_t max_pages_per_req,
+                            const int32_t* d_seq_lens, const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                            const int32_t* d_tp_page_table, void* stream) {
+  return reshard_kv_staged(u, 0, d_stage, stage_bytes, R, max_pages_per_req, d_seq_lens, d_ep_owner,
+                           d_ep_page_table, d_tp_page_table, stream);
+}
+
+int reshard_kv_tp2ep_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, int32_t R, int32_t max_pages_per_req,
+                            const int32_t* d_seq_lens, const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                            const int32_t* d_tp_page_table, void* stream) {
+  return reshard_kv_staged(u, 1, d_stage, stage_bytes, R, max_pages_per_req, d_seq_lens, d_ep_owner,
+                           d_ep_page_table, d_tp_page_table, stream);
 }
 
 int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,

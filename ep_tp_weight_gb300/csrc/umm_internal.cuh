@@ -86,11 +86,17 @@ struct Ws {
   int64_t bitmap_words;
   uint64_t tp_bitmap;  // uint32[(pages_tp+31)/32] TP source pages read by TP->EP
   uint64_t sched;      // uint64[pages_tp]      TP page -> (call << 32 | descriptor)
+  uint64_t order_tok;  // int64[max_requests]   staged path: token offsets in rank order
+  uint64_t rank_info;  // int64[3 * kMaxGroups] staged path: per-rank descriptor/token counts
   int32_t max_requests;
 };
 
 // ---- launchers (enqueue only; all arguments already validated) ----
 cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s);
+// The staged comparison path (permute + exchange through `stage`).
+uint64_t weights_stage_bytes(const Geo& g);
+cudaError_t launch_weights_staged(const Geo& g, int ep2tp, int layer, uint8_t* stage, cudaStream_t s,
+                                  int* launches);
 
 // use_sched: also index the descriptors by TP page (see launch_kv_copy).
 cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_t maxp,
@@ -101,6 +107,13 @@ cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_
 // exit at once); otherwise it walks the descriptor list.
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
                            unsigned int call, cudaStream_t s);
+
+// The staged comparison path for the KV cache (gather -> exchange -> scatter
+// per rank through `stage`; the descriptor pass must have run first).
+uint64_t kv_stage_bytes(const Geo& g);
+cudaError_t launch_kv_staged(const Geo& g, const Ws& w, int dir, int32_t R, const int32_t* lens,
+                             const int32_t* owner, uint8_t* stage, int64_t* order_tok, int64_t* rank_info,
+                             unsigned int call, cudaStream_t s, int sms, int* launches);
 
 cudaError_t launch_order(const Geo& g, const Ws& w, int32_t R, const int32_t* owner, int32_t* tp_pos,
                          unsigned int call, cudaStream_t s);

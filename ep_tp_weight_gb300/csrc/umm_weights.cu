@@ -16,10 +16,17 @@
 
 namespace uk {
 
+// TP-side addressing.  The fused path writes (reads) the TP slot of region q
+// itself: tp_base = buffer, q_stride = region stride, r_stride = 0,
+// expert offset r*El.  The staged path packs into per-peer blocks instead:
+// tp_base = staging, block (r, q) at (r*P + q)*block bytes, experts from 0.
 struct WParams {
   uint8_t* base;
   uint64_t region_stride, w13_off, w2_off;
-  uint64_t ep_slot_off, tp_slot_off;  // slot offsets inside a region
+  uint64_t ep_slot_off;               // EP slot offset inside a region
+  uint8_t* tp_base;
+  uint64_t tp_q_stride, tp_r_stride, tp_w13_off, tp_w2_off;
+  uint32_t tp_eoff_per_r;             // El (fused) or 0 (staged)
   uint64_t w13_row_bytes;             // H * 2
   uint64_t w2_tp_row_bytes;           // Ip * 2
   uint32_t El, Ip, H;
@@ -72,15 +79,15 @@ __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) 
         } else {
           p.two_ip.divmod(j, q, trow);
         }
-        const uint64_t e = (uint64_t)r * p.El + el;
-        tp_addr[u] = p.base + (uint64_t)q * p.region_stride + p.tp_slot_off + p.w13_off +
+        const uint64_t e = (uint64_t)r * p.tp_eoff_per_r + el;
+        tp_addr[u] = p.tp_base + (uint64_t)q * p.tp_q_stride + (uint64_t)r * p.tp_r_stride + p.tp_w13_off +
                      (e * 2 * p.Ip + trow) * p.w13_row_bytes + (uint64_t)hv * VB;
       } else {
         uint32_t row_all, iv, q, cc;
         p.iv.divmod(v - p.v13, row_all, iv);
         p.ipv.divmod(iv, q, cc);
-        const uint64_t trow = (uint64_t)r * p.El * p.H + row_all;
-        tp_addr[u] = p.base + (uint64_t)q * p.region_stride + p.tp_slot_off + p.w2_off +
+        const uint64_t trow = (uint64_t)r * p.tp_eoff_per_r * p.H + row_all;
+        tp_addr[u] = p.tp_base + (uint64_t)q * p.tp_q_stride + (uint64_t)r * p.tp_r_stride + p.tp_w2_off +
                      trow * p.w2_tp_row_bytes + (uint64_t)cc * VB;
       }
     }
@@ -118,13 +125,19 @@ cudaError_t run(const WParams& p, int ep2tp, cudaStream_t s) {
 }
 }  // namespace
 
-cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
+namespace {
+
+int vec_bytes(uint32_t H, uint32_t Ip) {
+  if (H % 8 == 0 && Ip % 8 == 0) return 16;
+  if (H % 4 == 0 && Ip % 4 == 0) return 8;
+  if (H % 2 == 0 && Ip % 2 == 0) return 4;
+  return 2;
+}
+
+// Parameters of one layer's permute: EP slot `layer`+1 <-> the TP side.
+WParams layer_params(const Geo& g, int layer, int VB) {
   const uint32_t El = (uint32_t)(g.E / g.P), Ip = (uint32_t)(g.I / g.P), H = (uint32_t)g.H;
   const uint32_t I = (uint32_t)g.I;
-  int VB = 2;
-  if (H % 8 == 0 && Ip % 8 == 0) VB = 16;
-  else if (H % 4 == 0 && Ip % 4 == 0) VB = 8;
-  else if (H % 2 == 0 && Ip % 2 == 0) VB = 4;
   const uint32_t per = (uint32_t)VB / 2;  // elements per vector
   WParams p;
   p.base = g.base;
@@ -132,7 +145,12 @@ cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   p.w13_off = g.w13_off;
   p.w2_off = g.w2_off;
   p.ep_slot_off = (uint64_t)(layer + 1) * g.wslot_stride;
-  p.tp_slot_off = (uint64_t)layer * g.wslot_stride;
+  p.tp_base = g.base;
+  p.tp_q_stride = g.region_stride;
+  p.tp_r_stride = 0;
+  p.tp_w13_off = (uint64_t)layer * g.wslot_stride + g.w13_off;
+  p.tp_w2_off = (uint64_t)layer * g.wslot_stride + g.w2_off;
+  p.tp_eoff_per_r = El;
   p.w13_row_bytes = (uint64_t)H * 2;
   p.w2_tp_row_bytes = (uint64_t)Ip * 2;
   p.El = El;
@@ -152,12 +170,122 @@ cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   p.ipv = FastDiv(Ip / per);
   p.tiles_per_region = FastDiv(tpr);
   p.split = g.w13_split;
+  return p;
+}
+
+cudaError_t run_any(const WParams& p, int VB, int ep2tp, cudaStream_t s) {
   switch (VB) {
     case 16: return run<16>(p, ep2tp, s);
     case 8: return run<8>(p, ep2tp, s);
     case 4: return run<4>(p, ep2tp, s);
     default: return run<2>(p, ep2tp, s);
   }
+}
+
+// Exchange stage of the staged path: block (r, q) of the staging buffer
+// holds, in TP layout, the W13 rows then the W2 rows that EP rank r's experts
+// contribute to TP rank q.  They are contiguous in TP rank q's slot too (its
+// experts r*El .. r*El+El-1), so the exchange is 2*P*P contiguous copies.
+struct XParams {
+  uint8_t* base;
+  const uint8_t* stage;
+  uint64_t region_stride, tp_w13_off, tp_w2_off;
+  uint64_t seg13, seg2, block;        // bytes: W13 part, W2 part, whole block
+  uint32_t P, tiles13, tiles2;        // 16 KiB tiles per part
+  uint32_t tiles_total;
+  FastDiv tiles_pair;                 // tiles13 + tiles2
+  FastDiv pd;                         // P
+};
+
+template <int VB, int U, int T>
+__global__ void __launch_bounds__(T) exchange_kernel(const XParams p, int to_tp) {
+  using V = typename VecT<VB>::T;
+  for (uint32_t tile = blockIdx.x; tile < p.tiles_total; tile += gridDim.x) {
+    uint32_t pair, lt, r, q;
+    p.tiles_pair.divmod(tile, pair, lt);
+    p.pd.divmod(pair, r, q);
+    const bool w13 = lt < p.tiles13;
+    const uint64_t seg = w13 ? p.seg13 : p.seg2;
+    const uint64_t off0 = (uint64_t)(w13 ? lt : lt - p.tiles13) * (uint64_t)(T * U * VB);
+    const uint8_t* st = p.stage + (uint64_t)pair * p.block + (w13 ? 0 : p.seg13);
+    uint8_t* tp = p.base + (uint64_t)q * p.region_stride +
+                  (w13 ? p.tp_w13_off + (uint64_t)r * p.seg13 : p.tp_w2_off + (uint64_t)r * p.seg2);
+    V val[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t o = off0 + (uint64_t)(u * T + threadIdx.x) * VB;
+      if (o < seg) val[u] = __ldcs(reinterpret_cast<const V*>((to_tp ? st : tp) + o));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t o = off0 + (uint64_t)(u * T + threadIdx.x) * VB;
+      if (o < seg) __stcs(reinterpret_cast<V*>(const_cast<uint8_t*>(to_tp ? tp : st) + o), val[u]);
+    }
+  }
+}
+
+cudaError_t run_exchange(const Geo& g, int layer, int VB, const uint8_t* stage, int to_tp, cudaStream_t s) {
+  const uint64_t El = (uint64_t)(g.E / g.P), Ip = (uint64_t)(g.I / g.P), H = (uint64_t)g.H;
+  XParams x;
+  x.base = g.base;
+  x.stage = stage;
+  x.region_stride = g.region_stride;
+  x.tp_w13_off = (uint64_t)layer * g.wslot_stride + g.w13_off;
+  x.tp_w2_off = (uint64_t)layer * g.wslot_stride + g.w2_off;
+  x.seg13 = El * 2 * Ip * H * 2;
+  x.seg2 = El * H * Ip * 2;
+  x.block = x.seg13 + x.seg2;
+  x.P = (uint32_t)g.P;
+  const uint64_t tb = (uint64_t)kT * kU * VB;
+  x.tiles13 = (uint32_t)((x.seg13 + tb - 1) / tb);
+  x.tiles2 = (uint32_t)((x.seg2 + tb - 1) / tb);
+  x.tiles_total = (x.tiles13 + x.tiles2) * x.P * x.P;
+  x.tiles_pair = FastDiv(x.tiles13 + x.tiles2);
+  x.pd = FastDiv(x.P);
+  if (x.tiles_total == 0) return cudaSuccess;
+  switch (VB) {
+    case 16: exchange_kernel<16, kU, kT><<<x.tiles_total, kT, 0, s>>>(x, to_tp); break;
+    case 8: exchange_kernel<8, kU, kT><<<x.tiles_total, kT, 0, s>>>(x, to_tp); break;
+    case 4: exchange_kernel<4, kU, kT><<<x.tiles_total, kT, 0, s>>>(x, to_tp); break;
+    default: exchange_kernel<2, kU, kT><<<x.tiles_total, kT, 0, s>>>(x, to_tp); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
+  const int VB = vec_bytes((uint32_t)g.H, (uint32_t)(g.I / g.P));
+  return run_any(layer_params(g, layer, VB), VB, ep2tp, s);
+}
+
+uint64_t weights_stage_bytes(const Geo& g) {
+  const uint64_t El = (uint64_t)(g.E / g.P), Ip = (uint64_t)(g.I / g.P), H = (uint64_t)g.H;
+  return (uint64_t)g.P * (uint64_t)g.P * (El * 2 * Ip * H * 2 + El * H * Ip * 2);
+}
+
+cudaError_t launch_weights_staged(const Geo& g, int ep2tp, int layer, uint8_t* stage, cudaStream_t s,
+                                  int* launches) {
+  const int VB = vec_bytes((uint32_t)g.H, (uint32_t)(g.I / g.P));
+  WParams p = layer_params(g, layer, VB);
+  const uint64_t El = (uint64_t)(g.E / g.P), Ip = (uint64_t)(g.I / g.P), H = (uint64_t)g.H;
+  const uint64_t block = El * 2 * Ip * H * 2 + El * H * Ip * 2;
+  p.tp_base = stage;
+  p.tp_q_stride = block;
+  p.tp_r_stride = (uint64_t)g.P * block;
+  p.tp_w13_off = 0;
+  p.tp_w2_off = El * 2 * Ip * H * 2;
+  p.tp_eoff_per_r = 0;
+  cudaError_t e;
+  if (ep2tp) {   // permute into per-peer blocks, then exchange into the TP slots
+    if ((e = run_any(p, VB, 1, s)) != cudaSuccess) return e;
+    e = run_exchange(g, layer, VB, stage, 1, s);
+  } else {       // exchange out of the TP slots, then permute into whole experts
+    if ((e = run_exchange(g, layer, VB, stage, 0, s)) != cudaSuccess) return e;
+    e = run_any(p, VB, 0, s);
+  }
+  *launches = 2;
+  return e;
 }
 
 }  // namespace uk

@@ -178,6 +178,20 @@ int reshard_weights_ep2tp(umm_t* u, void* stream);
 /* Inverse of the above, layers descending: TP slot l -> EP slot l+1. */
 int reshard_weights_tp2ep(umm_t* u, void* stream);
 
+/* The staged (collective-style) weight reshard, for comparison with the
+ * fused one (§4.3, Table 1: a collective path stages per-peer blocks and
+ * touches HBM twice; the fused path once).  EP->TP permutes each EP rank's
+ * slot into per-peer blocks in `d_stage`, then an exchange copies block
+ * (r, q) into TP rank q's slot; TP->EP runs the exchange out of the TP slots,
+ * then the permute back into whole experts.  Two reads and two writes per
+ * element; same result as the fused calls.  `d_stage`: caller-owned device
+ * memory, 256-byte aligned, at least umm_weights_stage_bytes() bytes
+ * (P*P blocks, one layer).  Errors as the fused calls, plus ALIGN and
+ * CAPACITY (staging too small). */
+int umm_weights_stage_bytes(const umm_t* u, uint64_t* bytes_out);
+int reshard_weights_ep2tp_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, void* stream);
+int reshard_weights_tp2ep_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, void* stream);
+
 /* §3.2 EP -> TP request order (metadata all-gather): the global list is rank
  * 0's requests, then rank 1's, ..., each rank's in ascending request index.
  * d_tp_pos[k] receives request k's position.  d_ep_owner[k] in [0, P).
@@ -254,6 +268,23 @@ int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
 int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
                      const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
                      const int32_t* d_tp_page_table, void* stream);
+
+/* The staged (collective-style) KV reshard, for comparison with the fused
+ * one (§3.2: gather scattered token slots into per-peer contiguous blocks,
+ * exchange them once, scatter into the target pages; §4.3, Table 1).  Same
+ * arguments and result as the fused calls; each layer moves one EP rank at a
+ * time through `d_stage` (caller-owned device memory, 256-byte aligned, at
+ * least umm_kv_stage_bytes(): a send and a receive area for one rank's live
+ * tokens at full EP capacity).  Every replicated row crosses HBM three times
+ * (gather, exchange, scatter) instead of once.  Errors as the fused calls,
+ * plus ALIGN and CAPACITY (staging too small). */
+int umm_kv_stage_bytes(const umm_t* u, uint64_t* bytes_out);
+int reshard_kv_ep2tp_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, int32_t R, int32_t max_pages_per_req,
+                            const int32_t* d_seq_lens, const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                            const int32_t* d_tp_page_table, void* stream);
+int reshard_kv_tp2ep_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, int32_t R, int32_t max_pages_per_req,
+                            const int32_t* d_seq_lens, const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
+                            const int32_t* d_tp_page_table, void* stream);
 
 /* §4.5 capacity check on the host, before committing a switch: UMM_OK if the
  * target layout's KV pools hold the requests (TP: all pages in one pool of

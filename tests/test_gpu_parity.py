@@ -314,3 +314,53 @@ def test_switch_captured_in_a_cuda_graph():
     np.testing.assert_array_equal(dev.host(), ref)
     assert dev.status() == (0, 0)
     dev.close()
+
+
+# ------------------------------------------------------------------ staged (collective-style) comparison path
+
+@pytest.mark.parametrize("w", [TINY, W_CASES[1], W_CASES[3], W_CASES[5]], ids=lambda w: w.name)
+def test_weights_staged_equals_oracle(w):
+    """The staged path (permute into per-peer blocks + exchange) lands the
+    same bytes as the definition."""
+    dev = DevUMM(w, seed=13)
+    nb = umm.umm_weights_stage_bytes(dev.h)
+    stage = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    ref = dev.host()
+    umm.reshard_weights_ep2tp_staged(dev.h, stage, nb)
+    oracle.weights_ep2tp(ref, dev.d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    umm.reshard_weights_tp2ep_staged(dev.h, stage, nb)
+    oracle.weights_tp2ep(ref, dev.d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    with pytest.raises(umm.UmmError) as ei:
+        umm.reshard_weights_ep2tp_staged(dev.h, stage, nb - 16)
+    assert ei.value.code == umm.UMM_ERR_CAPACITY
+    dev.close()
+
+
+@pytest.mark.parametrize("w", KV_CASES, ids=lambda w: w.name)
+def test_kv_staged_equals_oracle(w):
+    """The staged KV path (gather into per-peer blocks, exchange, scatter)
+    lands the same bytes as the definition, both directions."""
+    dev = DevUMM(w, seed=14)
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=5)
+    nb = umm.umm_kv_stage_bytes(dev.h)
+    stage = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    ref = dev.host()
+    maxp = st.ep_pt.shape[1]
+    g = lambda a: i32(a)
+    umm.reshard_kv_ep2tp_staged(dev.h, stage, nb, len(st.lens), maxp, g(st.lens), g(st.owner), g(st.ep_pt),
+                                g(st.tp_pt))
+    assert oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+    free2 = synth.permutation(8, 4, L["pages_ep"], rows=d.P)
+    _, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, maxp, free2, region=owner2, key=st.tp_pos)
+    umm.reshard_kv_tp2ep_staged(dev.h, stage, nb, len(st.lens), maxp, g(st.lens), g(owner2), g(ep_pt2),
+                                g(st.tp_pt))
+    assert oracle.kv_tp2ep(ref, d, st.lens, owner2, ep_pt2, st.tp_pt) == 0
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
