@@ -80,8 +80,16 @@ def algorithmic_bytes(w, lens) -> dict:
         out["kv_ep2tp_per_layer"] = rd + wr
         out["kv_tp2ep_per_layer"] = 2 * rd
         out["tokens"] = T
+    if w.Hq:
+        hq, h_tp = w.Hq // w.P, w.h_tp
+        shard = ((hq + 2 * h_tp) * w.D * w.H + w.H * hq * w.D) * 2          # one rank's TP shard, bytes
+        full = ((w.Hq + 2 * w.Hkv) * w.D * w.H + w.H * w.Hq * w.D) * 2     # one full copy
+        out["attn_ep2tp_per_layer"] = 2 * w.P * shard                       # every rank keeps its shard
+        out["attn_tp2ep_per_layer"] = full + w.P * full                     # read each element once, write P copies
     step = 2 * out.get("weights_per_switch", 0) + w.N * (out.get("kv_ep2tp_per_layer", 0) +
-                                                        out.get("kv_tp2ep_per_layer", 0))
+                                                        out.get("kv_tp2ep_per_layer", 0) +
+                                                        out.get("attn_ep2tp_per_layer", 0) +
+                                                        out.get("attn_tp2ep_per_layer", 0))
     out["step"] = step
     return out
 
@@ -228,7 +236,7 @@ def run_umm(args, rank, world, local_rank):
     d = w.dims()
     dims = umm.make_dims(P=d["P"], E=d["E"], H=d["H"], I=d["I"], N=d["N"], Hkv=d["Hkv"], D=d["D"],
                          ps=d["ps"], pages_tp=d["pages_tp"], max_requests=d["max_requests"],
-                         max_pages=d["max_pages"])
+                         max_pages=d["max_pages"], Hq=d.get("Hq", 0))
     nbytes = umm.umm_required_bytes(dims)
     buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)          # the one allocation (§4.2)
     h = umm.umm_create(dims, buf, nbytes)
@@ -277,6 +285,8 @@ def run_umm(args, rank, world, local_rank):
         e0 = torch.cuda.Event(enable_timing=True) if mark else None
         if mark:
             e0.record(s)
+        if w.Hq:
+            umm.reshard_attn_ep2tp(h, s)
         if w.E:
             umm.reshard_weights_ep2tp(h, s)
         if have_kv:
@@ -293,6 +303,8 @@ def run_umm(args, rank, world, local_rank):
                                  state["ep_pt_n"], maxp, s)
         if w.E:
             umm.reshard_weights_tp2ep(h, s)
+        if w.Hq:
+            umm.reshard_attn_tp2ep(h, s)
         if have_kv:
             umm.reshard_kv_tp2ep(h, R, maxp, lens, state["owner_n"], state["ep_pt_n"], tp_pt, s)
             state["owner"], state["owner_n"] = state["owner_n"], state["owner"]
@@ -497,6 +509,13 @@ class CpuSample:
         self.threads = threads
         self.wbuf = None
         self.kbuf = None
+        self.abuf = None
+        if w.Hq:
+            aw = w.with_(E=0, R=0)
+            self.ad = oracle.Dims(**aw.dims())
+            self.abuf = np.ones(oracle.layout(self.ad)["ws_off"], dtype=np.uint8)
+            b = algorithmic_bytes(aw, [])
+            self.abytes = w.N * (b["attn_ep2tp_per_layer"] + b["attn_tp2ep_per_layer"])
         if w.E:
             ws = w.with_(Hkv=0, R=0)
             self.wd = oracle.Dims(**ws.dims())
@@ -523,14 +542,26 @@ class CpuSample:
         self.n_runs = 0
 
     def describe(self) -> str:
-        return (f"plain C oracle (element by element, OpenMP, {self.threads} threads): expert weights of all "
-                f"{self.w.N} layers EP->TP->EP + KV of the first {min(self.KV_REQUESTS, self.w.R)} of "
-                f"{self.w.R} requests for 1 layer EP->TP->EP")
+        parts = []
+        if self.abuf is not None:
+            parts.append(f"attention weights of all {self.w.N} layers EP->TP->EP")
+        if self.wbuf is not None:
+            parts.append(f"expert weights of all {self.w.N} layers EP->TP->EP")
+        if self.kbuf is not None:
+            parts.append(f"KV of the first {min(self.KV_REQUESTS, self.w.R)} of {self.w.R} requests for 1 layer "
+                         f"EP->TP->EP")
+        return f"plain C oracle (element by element, OpenMP, {self.threads} threads): " + " + ".join(parts)
 
     def run(self):
         """One sample; returns (algorithmic bytes, seconds of oracle work)."""
         o, w = self.oracle, self.w
         moved, secs = 0, 0.0
+        if self.abuf is not None:
+            t = time.perf_counter()
+            o.attn_ep2tp(self.abuf, self.ad)
+            o.attn_tp2ep(self.abuf, self.ad)
+            secs += time.perf_counter() - t
+            moved += self.abytes
         if self.wbuf is not None:
             t = time.perf_counter()
             o.weights_ep2tp(self.wbuf, self.wd)
@@ -572,7 +603,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     w = ALL[args.workload]
-    config = {"workload": w.name, "P": w.P, "layers": w.N, "experts": w.E, "hidden": w.H,
+    config = {"workload": w.name, "P": w.P, "layers": w.N, "experts": w.E, "hidden": w.H, "attn_q_heads": w.Hq,
               "intermediate": w.I, "requests": w.R, "kv_heads": w.Hkv, "head_dim": w.D, "page_size": w.ps,
               "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas{world}"}
 
@@ -618,7 +649,9 @@ def main():
     n_dom, ms_dom = prof[dom]
     per_launch_bytes = {"kv_ep2tp": b.get("kv_ep2tp_per_layer", 0), "kv_tp2ep": b.get("kv_tp2ep_per_layer", 0),
                         "weights_ep2tp": b.get("weights_per_layer", 0),
-                        "weights_tp2ep": b.get("weights_per_layer", 0)}.get(dom, 0)
+                        "weights_tp2ep": b.get("weights_per_layer", 0),
+                        "attn_ep2tp": b.get("attn_ep2tp_per_layer", 0),
+                        "attn_tp2ep": b.get("attn_tp2ep_per_layer", 0)}.get(dom, 0)
     achieved = per_launch_bytes / (ms_dom / n_dom / 1e3) / 1e9 if n_dom else 0.0
     kernel_name = {"kv_ep2tp": "kv_copy_ep2tp", "kv_tp2ep": "kv_copy_tp2ep", "weights_ep2tp": "weights_kernel",
                    "weights_tp2ep": "weights_kernel"}.get(dom)
@@ -627,7 +660,8 @@ def main():
     per_kind = {k: {"launches": n, "ms_per_launch": round(ms / n, 4) if n else None}
                 for k, (n, ms) in prof.items() if n}
     for k, key in (("weights_ep2tp", "weights_per_layer"), ("weights_tp2ep", "weights_per_layer"),
-                   ("kv_ep2tp", "kv_ep2tp_per_layer"), ("kv_tp2ep", "kv_tp2ep_per_layer")):
+                   ("kv_ep2tp", "kv_ep2tp_per_layer"), ("kv_tp2ep", "kv_tp2ep_per_layer"),
+                   ("attn_ep2tp", "attn_ep2tp_per_layer"), ("attn_tp2ep", "attn_tp2ep_per_layer")):
         if k in per_kind and b.get(key):
             gbs = b[key] / (per_kind[k]["ms_per_launch"] / 1e3) / 1e9
             per_kind[k]["GB_s"] = round(gbs, 1)
@@ -639,7 +673,8 @@ def main():
         "config": config,
         "ms_per_switch": {"ep2tp": round(r["ms_ep2tp"], 3), "tp2ep": round(r["ms_tp2ep"], 3)},
         "ms_per_layer": {k: per_kind[k]["ms_per_launch"] for k in ("weights_ep2tp", "weights_tp2ep", "kv_ep2tp",
-                                                                   "kv_tp2ep") if k in per_kind},
+                                                                   "kv_tp2ep", "attn_ep2tp", "attn_tp2ep")
+                         if k in per_kind},
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "frac_of_8TBs_nominal": round(value / world / 8000.0, 4),
         "bytes_per_step": b["step"], "tokens": b.get("tokens"),

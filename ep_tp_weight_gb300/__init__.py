@@ -33,9 +33,11 @@ FLAG_CAPACITY = 2
 FLAG_PAGE_OOB = 4
 FLAG_DUP_PAGE = 8
 
-K_WEIGHTS_EP2TP, K_WEIGHTS_TP2EP, K_KV_PREP, K_KV_EP2TP, K_KV_TP2EP, K_PLACE, K_ORDER, K_ASSIGN = range(8)
-K_COUNT = 8
-KIND_NAMES = ("weights_ep2tp", "weights_tp2ep", "kv_prep", "kv_ep2tp", "kv_tp2ep", "place", "order", "assign")
+(K_WEIGHTS_EP2TP, K_WEIGHTS_TP2EP, K_KV_PREP, K_KV_EP2TP, K_KV_TP2EP, K_PLACE, K_ORDER, K_ASSIGN,
+ K_ATTN_EP2TP, K_ATTN_TP2EP) = range(10)
+K_COUNT = 10
+KIND_NAMES = ("weights_ep2tp", "weights_tp2ep", "kv_prep", "kv_ep2tp", "kv_tp2ep", "place", "order", "assign",
+              "attn_ep2tp", "attn_tp2ep")
 
 
 class UmmDims(ctypes.Structure):
@@ -43,7 +45,7 @@ class UmmDims(ctypes.Structure):
                 ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("kv_pages_tp", ctypes.c_int64), ("max_requests", ctypes.c_int32),
                 ("w13_split", ctypes.c_int32), ("max_pages", ctypes.c_int64), ("weight_mode", ctypes.c_int32),
-                ("kv_mode", ctypes.c_int32)]
+                ("kv_mode", ctypes.c_int32), ("attn_q_heads", ctypes.c_int32), ("attn_mode", ctypes.c_int32)]
 
 
 class UmmLayout(ctypes.Structure):
@@ -51,7 +53,8 @@ class UmmLayout(ctypes.Structure):
                                                "kvslot_stride", "kv_v_off", "kvslots_off", "ws_off",
                                                "ws_bytes", "total_bytes")] + \
                [(n, ctypes.c_int64) for n in ("pages_ep", "pages_tp", "h_tp")] + \
-               [("status_off", ctypes.c_uint64), ("desc_off", ctypes.c_uint64), ("desc_capacity", ctypes.c_int64)]
+               [("status_off", ctypes.c_uint64), ("desc_off", ctypes.c_uint64), ("desc_capacity", ctypes.c_int64)] + \
+               [(n, ctypes.c_uint64) for n in ("attnslot_stride", "attn_wo_off", "attnslots_off")]
 
     def as_dict(self) -> dict:
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -106,6 +109,10 @@ _SIG = {
     "umm_kv_stage_bytes": [_vp, _P(_u64)],
     "reshard_kv_ep2tp_staged": [_vp, _vp, _u64, _i32, _i32, _vp, _vp, _vp, _vp, _vp],
     "reshard_kv_tp2ep_staged": [_vp, _vp, _u64, _i32, _i32, _vp, _vp, _vp, _vp, _vp],
+    "reshard_attn_ep2tp": [_vp, _vp],
+    "reshard_attn_tp2ep": [_vp, _vp],
+    "umm_get_attn_mode": [_vp, _P(_i32)],
+    "umm_set_attn_mode": [_vp, _i32],
     "umm_policy_create": [_vp, _P(_vp)],
     "umm_policy_destroy": [_vp],
     "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
@@ -148,10 +155,11 @@ def _stream(s):
 
 
 def make_dims(P, E=0, H=0, I=0, N=1, Hkv=0, D=0, ps=16, pages_tp=0, max_requests=0, max_pages=0,
-              w13_split=0, weight_mode=UMM_MODE_EP, kv_mode=UMM_MODE_EP) -> UmmDims:
+              w13_split=0, weight_mode=UMM_MODE_EP, kv_mode=UMM_MODE_EP, Hq=0,
+              attn_mode=UMM_MODE_EP) -> UmmDims:
     """umm_dims from the page's notation (§3.1, §3.2)."""
     return UmmDims(P, E, H, I, N, Hkv, D, ps, pages_tp, max_requests, w13_split, max_pages,
-                   weight_mode, kv_mode)
+                   weight_mode, kv_mode, Hq, attn_mode)
 
 
 def umm_required_bytes(dims: UmmDims) -> int:
@@ -234,6 +242,24 @@ def reshard_kv_tp2ep_staged(h: int, stage, stage_bytes: int, R: int, max_pages_p
     _ck(_lib.reshard_kv_tp2ep_staged(h, _ptr(stage), int(stage_bytes), R, max_pages_per_req, _ptr(seq_lens),
                                      _ptr(ep_owner), _ptr(ep_page_table), _ptr(tp_page_table), _stream(stream)),
         "reshard_kv_tp2ep_staged")
+
+
+def reshard_attn_ep2tp(h: int, stream=None) -> None:
+    _ck(_lib.reshard_attn_ep2tp(h, _stream(stream)), "reshard_attn_ep2tp")
+
+
+def reshard_attn_tp2ep(h: int, stream=None) -> None:
+    _ck(_lib.reshard_attn_tp2ep(h, _stream(stream)), "reshard_attn_tp2ep")
+
+
+def umm_get_attn_mode(h: int) -> int:
+    m = ctypes.c_int32()
+    _ck(_lib.umm_get_attn_mode(h, ctypes.byref(m)), "umm_get_attn_mode")
+    return m.value
+
+
+def umm_set_attn_mode(h: int, mode: int) -> None:
+    _ck(_lib.umm_set_attn_mode(h, mode), "umm_set_attn_mode")
 
 
 def gather_requests_ep2tp(h: int, R: int, ep_owner, tp_pos, stream=None) -> None:

@@ -39,7 +39,7 @@ struct umm {
   uk::Ws ws;
   int device = 0;
   int sms = 1;
-  int32_t weight_mode = UMM_MODE_EP, kv_mode = UMM_MODE_EP;
+  int32_t weight_mode = UMM_MODE_EP, kv_mode = UMM_MODE_EP, attn_mode = UMM_MODE_EP;
   unsigned int next_call = 0;
   std::vector<KvCall> kv_log;
   bool prof = false;
@@ -76,8 +76,18 @@ int check_dims(const umm_dims* d) {
   if (d->max_pages < 0 || d->max_pages >= (1ll << 31)) return UMM_ERR_INVALID_ARG;
   if (d->w13_split != 0 && d->w13_split != 1) return UMM_ERR_INVALID_ARG;
   if ((d->weight_mode != UMM_MODE_EP && d->weight_mode != UMM_MODE_TP) ||
-      (d->kv_mode != UMM_MODE_EP && d->kv_mode != UMM_MODE_TP))
+      (d->kv_mode != UMM_MODE_EP && d->kv_mode != UMM_MODE_TP) ||
+      (d->attn_mode != UMM_MODE_EP && d->attn_mode != UMM_MODE_TP))
     return UMM_ERR_INVALID_ARG;
+  if (d->attn_q_heads < 0) return UMM_ERR_INVALID_ARG;
+  if (d->attn_q_heads > 0) {
+    if (d->num_kv_heads < 1 || d->head_dim < 1 || d->H < 1 || d->attn_q_heads % d->P) return UMM_ERR_INVALID_ARG;
+    const uint64_t hq = (uint64_t)(d->attn_q_heads / d->P);
+    const uint64_t h_tp = (uint64_t)(d->num_kv_heads >= d->P ? d->num_kv_heads / d->P : 1);
+    // per-rank shard element count must stay addressable by 32-bit vector indices
+    if ((hq + 2 * h_tp) * d->head_dim * (uint64_t)d->H + (uint64_t)d->H * hq * d->head_dim >= (1ull << 31) - (1ull << 16))
+      return UMM_ERR_INVALID_ARG;
+  }
   return UMM_OK;
 }
 
@@ -101,7 +111,13 @@ void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
   L->kv_v_off = align_up(half, 256);
   L->kvslot_stride = hkv > 0 ? align_up(L->kv_v_off + half, 4096) : 0;
   L->kvslots_off = (N + 1) * L->wslot_stride;
-  L->region_stride = align_up((N + 1) * (L->wslot_stride + L->kvslot_stride), 2ull << 20);
+  // attention slots (R-16), sized for the full EP copy
+  const uint64_t hq = (uint64_t)d->attn_q_heads;
+  const uint64_t qkv = hq > 0 ? (hq + 2ull * (uint64_t)hkv) * d->head_dim * (uint64_t)d->H * 2ull : 0;
+  L->attn_wo_off = align_up(qkv, 256);
+  L->attnslot_stride = hq > 0 ? align_up(L->attn_wo_off + (uint64_t)d->H * hq * d->head_dim * 2ull, 4096) : 0;
+  L->attnslots_off = (N + 1) * (L->wslot_stride + L->kvslot_stride);
+  L->region_stride = align_up((N + 1) * (L->wslot_stride + L->kvslot_stride + L->attnslot_stride), 2ull << 20);
   L->ws_off = P * L->region_stride;
 
   const int64_t desc_cap = d->max_pages > 0 ? d->max_pages : L->pages_tp;
@@ -356,11 +372,16 @@ int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) 
   g.D = dims->head_dim;
   g.ps = dims->page_size;
   g.w13_split = dims->w13_split;
+  g.Hq = dims->attn_q_heads;
+  g.attnslot_stride = u->L.attnslot_stride;
+  g.attn_wo_off = u->L.attn_wo_off;
+  g.attnslots_off = u->L.attnslots_off;
   g.pages_ep = u->L.pages_ep;
   g.pages_tp = u->L.pages_tp;
   g.h_tp = u->L.h_tp;
   u->weight_mode = dims->weight_mode;
   u->kv_mode = dims->kv_mode;
+  u->attn_mode = dims->attn_mode;
   // status block and TP-page schedule start at zero (call id 0 is never used)
   if (cudaMemset(g.base + u->ws.status, 0, kStatusBytes) != cudaSuccess ||
       (u->L.pages_tp > 0 && cudaMemset(g.base + u->ws.sched, 0, (size_t)u->L.pages_tp * 8) != cudaSuccess) ||
@@ -404,6 +425,37 @@ int umm_set_modes(umm_t* u, int32_t weight_mode, int32_t kv_mode) {
   u->weight_mode = weight_mode;
   u->kv_mode = kv_mode;
   u->kv_log.clear();
+  return UMM_OK;
+}
+
+int reshard_attn(umm_t* u, int ep2tp, void* stream) {
+  if (!u || u->dims.attn_q_heads == 0) return UMM_ERR_INVALID_ARG;
+  if (u->attn_mode != (ep2tp ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
+  cudaStream_t s = as_stream(stream);
+  const int N = u->dims.num_layers;
+  for (int t = 0; t < N; ++t) {
+    const int layer = ep2tp ? t : N - 1 - t;
+    ProfScope ps(u, ep2tp ? UMM_K_ATTN_EP2TP : UMM_K_ATTN_TP2EP, s);
+    int rc = cuda_rc(uk::launch_attn(u->geo, ep2tp, layer, s));
+    if (rc) return rc;
+    ++u->launches;
+  }
+  u->attn_mode = ep2tp ? UMM_MODE_TP : UMM_MODE_EP;
+  return UMM_OK;
+}
+
+int reshard_attn_ep2tp(umm_t* u, void* stream) { return reshard_attn(u, 1, stream); }
+int reshard_attn_tp2ep(umm_t* u, void* stream) { return reshard_attn(u, 0, stream); }
+
+int umm_get_attn_mode(const umm_t* u, int32_t* mode) {
+  if (!u || !mode) return UMM_ERR_INVALID_ARG;
+  *mode = u->attn_mode;
+  return UMM_OK;
+}
+
+int umm_set_attn_mode(umm_t* u, int32_t mode) {
+  if (!u || (mode != UMM_MODE_EP && mode != UMM_MODE_TP)) return UMM_ERR_INVALID_ARG;
+  u->attn_mode = mode;
   return UMM_OK;
 }
 

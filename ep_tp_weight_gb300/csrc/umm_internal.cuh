@@ -68,8 +68,9 @@ struct Geo {
   uint8_t* base;
   uint64_t region_stride, wslot_stride, w13_off, w2_off;
   uint64_t kvslot_stride, kv_v_off, kvslots_off;
-  int32_t P, E, H, I, N, Hkv, D, ps, w13_split;
+  int32_t P, E, H, I, N, Hkv, D, ps, w13_split, Hq;
   int64_t pages_ep, pages_tp, h_tp;
+  uint64_t attnslot_stride, attn_wo_off, attnslots_off;
 };
 
 // Workspace carve-up (byte offsets from the buffer base).
@@ -92,6 +93,7 @@ struct Ws {
 };
 
 // ---- launchers (enqueue only; all arguments already validated) ----
+cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s);
 cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s);
 // The staged comparison path (permute + exchange through `stage`).
 uint64_t weights_stage_bytes(const Geo& g);

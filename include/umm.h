@@ -91,6 +91,10 @@ typedef struct {
                               (0 = kv_pages_tp)                                      */
   int32_t weight_mode;     /* layout the weights are in at create (UMM_MODE_*)      */
   int32_t kv_mode;         /* layout the KV cache is in at create                   */
+  int32_t attn_q_heads;    /* Hq query heads of the attention weights kept in the
+                              memory-saving layout (0 = none); needs
+                              num_kv_heads, head_dim, H and Hq % P == 0          */
+  int32_t attn_mode;       /* layout the attention weights are in at create       */
 } umm_dims;
 
 /* ---- buffer layout (all offsets in bytes from the buffer base) ----
@@ -103,6 +107,11 @@ typedef struct {
  *       K half at +0, V half at +kv_v_off; each half is a page pool
  *       EP view of layer l = slot l+1: [pages_ep][page_size][num_kv_heads][head_dim]
  *       TP view of layer l = slot l:   [pages_tp][page_size][h_tp][head_dim]
+ *   attention slot s (s = 0..N) at r*region_stride + attnslots_off + s*attnslot_stride
+ *       (only with attn_q_heads > 0): Wqkv at +0, Wo at +attn_wo_off;
+ *       EP view of layer l = slot l+1: Wqkv [Hq + 2*Hkv heads][Dh][H], Wo [H][Hq*Dh]
+ *       TP view of layer l = slot l:   Wqkv [Hq/P + 2*h_tp heads][Dh][H] (rank q's
+ *       query heads, then its key heads, then its value heads), Wo [H][Hq/P*Dh]
  * The workspace (status, descriptors, scratch) follows the P regions at
  * ws_off; callers must not write it.  total_bytes = ws_off + ws_bytes. */
 typedef struct {
@@ -113,6 +122,7 @@ typedef struct {
   uint64_t status_off;     /* umm_status_block                                      */
   uint64_t desc_off;       /* umm_kv_desc[desc_capacity]                             */
   int64_t desc_capacity;
+  uint64_t attnslot_stride, attn_wo_off, attnslots_off;
 } umm_layout_t;
 
 /* Workspace status block (device memory, at status_off). */
@@ -177,6 +187,19 @@ int reshard_weights_ep2tp(umm_t* u, void* stream);
 
 /* Inverse of the above, layers descending: TP slot l -> EP slot l+1. */
 int reshard_weights_tp2ep(umm_t* u, void* stream);
+
+/* §3.1, memory-saving variant of the attention weights (only the active
+ * layout is resident).  EP->TP: every rank keeps its own shard of its full
+ * copy (query heads q*Hq/P.., its key and value heads, its Wo columns);
+ * nothing crosses ranks.  TP->EP: all-gather -- every rank's full copy is
+ * rebuilt from the shards, key/value heads from their lowest replica; each
+ * shard element is read once and written to all P ranks.  One launch per
+ * layer (ascending / descending, N+1 slots as for the expert weights).
+ * Errors: INVALID_ARG (no attention weights), MODE, CUDA. */
+int reshard_attn_ep2tp(umm_t* u, void* stream);
+int reshard_attn_tp2ep(umm_t* u, void* stream);
+int umm_get_attn_mode(const umm_t* u, int32_t* mode);
+int umm_set_attn_mode(umm_t* u, int32_t mode);
 
 /* The staged (collective-style) weight reshard, for comparison with the
  * fused one (§4.3, Table 1: a collective path stages per-peer blocks and
@@ -313,7 +336,9 @@ const char* umm_strerror(int code);
 #define UMM_K_PLACE         5
 #define UMM_K_ORDER         6
 #define UMM_K_ASSIGN        7
-#define UMM_K_COUNT         8
+#define UMM_K_ATTN_EP2TP    8
+#define UMM_K_ATTN_TP2EP    9
+#define UMM_K_COUNT         10
 int umm_profile_enable(umm_t* u, int32_t enable);
 /* Synchronises the recorded events; launches and summed milliseconds of one
  * kind since the last reset. */

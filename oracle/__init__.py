@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.orc_layout.argtypes = [vp, vp]
         for f in ("orc_weights_ep2tp", "orc_weights_tp2ep"):
             getattr(L, f).argtypes = [vp, vp, vp, i32]
+        for f in ("orc_attn_ep2tp", "orc_attn_tp2ep"):
+            getattr(L, f).argtypes = [vp, vp, vp, i32]
         L.orc_w13_tp_elem.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp, vp]
         L.orc_w2_tp_elem.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp, vp]
         L.orc_kv_validate.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp]
@@ -87,6 +89,7 @@ class Dims:
     max_requests: int = 0
     max_pages: int = 0
     w13_split: int = 0
+    Hq: int = 0           # attention query heads (0 = no attention weights)
 
     def vec(self) -> np.ndarray:
         return np.array([getattr(self, f.name) for f in fields(self)], dtype=np.int64)
@@ -101,7 +104,8 @@ class Dims:
 
 
 LAYOUT_KEYS = ("region_stride", "wslot_stride", "w13_off", "w2_off", "kvslot_stride",
-               "kv_v_off", "kvslots_off", "ws_off", "pages_ep", "pages_tp", "h_tp")
+               "kv_v_off", "kvslots_off", "ws_off", "pages_ep", "pages_tp", "h_tp",
+               "attnslot_stride", "attn_wo_off", "attnslots_off")
 
 
 def layout(d: Dims) -> dict:
@@ -139,6 +143,18 @@ def weights_ep2tp(buf: np.ndarray, d: Dims, src: np.ndarray | None = None, order
 def weights_tp2ep(buf: np.ndarray, d: Dims, src: np.ndarray | None = None, order: int = -1) -> None:
     dv = d.vec()
     lib().orc_weights_tp2ep(_ptr(src if src is not None else buf), _ptr(buf), dv.ctypes.data, order)
+
+
+def attn_ep2tp(buf: np.ndarray, d: Dims, src: np.ndarray | None = None, order: int = 1) -> None:
+    """Attention weights EP -> TP (keep own shard), memory-saving variant."""
+    dv = d.vec()
+    lib().orc_attn_ep2tp(_ptr(src if src is not None else buf), _ptr(buf), dv.ctypes.data, order)
+
+
+def attn_tp2ep(buf: np.ndarray, d: Dims, src: np.ndarray | None = None, order: int = -1) -> None:
+    """Attention weights TP -> EP (all-gather of the shards)."""
+    dv = d.vec()
+    lib().orc_attn_tp2ep(_ptr(src if src is not None else buf), _ptr(buf), dv.ctypes.data, order)
 
 
 def w13_tp_elem(d: Dims, q, e, row, h, ep_slot, tp_slot):

@@ -38,6 +38,14 @@
  *   R-6 local order inside an EP rank = ascending list key.
  *   R-7 pages are handed out in list order from a caller-given free list.
  *   R-8 bytes that are not a destination keep their previous contents.
+ *   R-16 attention weights (§3.1, memory-saving variant: only the active
+ *       layout is kept; TP->EP rebuilds it with an all-gather).  EP (DP
+ *       attention): every rank holds the full Wqkv = [Hq query heads][Hkv key
+ *       heads][Hkv value heads], each head Dh rows of H, and Wo [H][Hq*Dh].
+ *       TP: rank q holds query heads [q*Hq/P, (q+1)*Hq/P), its KV heads (R-3)
+ *       for K then V, and the Wo columns of its query heads.  Both views use
+ *       the same offsets inside an attention slot (Wqkv at 0, Wo at a
+ *       256-byte boundary after the full Wqkv); N+1 slots as for the weights.
  *
  * All data is moved as raw bytes (bf16 = 2 opaque bytes); nothing passes
  * through floating point.
@@ -52,12 +60,12 @@
 /* ---- dims / layout vectors exchanged with the Python wrapper (int64) ---- */
 enum {
   OD_P, OD_E, OD_H, OD_I, OD_N, OD_HKV, OD_HD, OD_PS, OD_PAGES_TP,
-  OD_MAX_REQ, OD_MAX_PAGES, OD_W13_SPLIT, OD_COUNT
+  OD_MAX_REQ, OD_MAX_PAGES, OD_W13_SPLIT, OD_HQ, OD_COUNT
 };
 enum {
   OL_REGION_STRIDE, OL_WSLOT_STRIDE, OL_W13_OFF, OL_W2_OFF, OL_KVSLOT_STRIDE,
   OL_KV_V_OFF, OL_KVSLOTS_OFF, OL_WS_OFF, OL_PAGES_EP, OL_PAGES_TP, OL_H_TP,
-  OL_COUNT
+  OL_ATTN_STRIDE, OL_ATTN_WO_OFF, OL_ATTNSLOTS_OFF, OL_COUNT
 };
 
 /* error flags the oracle expects a KV/assign call to raise (bit values) */
@@ -91,7 +99,11 @@ void orc_layout(const int64_t *d, int64_t *L) {
   int64_t half = (Hkv > 0) ? pages_tp * ps * h_tp * D * 2 : 0;
   int64_t v_off = round_up(half, 256);
   int64_t kvslot = (Hkv > 0) ? round_up(v_off + half, 4096) : 0;
-  int64_t region = round_up((N + 1) * (wslot + kvslot), (int64_t)2 << 20);
+  int64_t Hq = d[OD_HQ];
+  int64_t qkv = (Hq > 0) ? (Hq + 2 * Hkv) * D * H * 2 : 0;     /* full Wqkv bytes */
+  int64_t wo_off = round_up(qkv, 256);
+  int64_t attnslot = (Hq > 0) ? round_up(wo_off + H * Hq * D * 2, 4096) : 0;
+  int64_t region = round_up((N + 1) * (wslot + kvslot + attnslot), (int64_t)2 << 20);
   memset(L, 0, sizeof(int64_t) * OL_COUNT);
   L[OL_REGION_STRIDE] = region;
   L[OL_WSLOT_STRIDE] = wslot;
@@ -104,6 +116,9 @@ void orc_layout(const int64_t *d, int64_t *L) {
   L[OL_PAGES_EP] = (Hkv > 0) ? pages_tp * h_tp / Hkv : 0;
   L[OL_PAGES_TP] = pages_tp;
   L[OL_H_TP] = (Hkv > 0) ? h_tp : 0;
+  L[OL_ATTN_STRIDE] = attnslot;
+  L[OL_ATTN_WO_OFF] = wo_off;
+  L[OL_ATTNSLOTS_OFF] = (N + 1) * (wslot + kvslot);
 }
 
 /* byte offset of weight slot s of region r */
@@ -423,6 +438,82 @@ void orc_kv_elem(const int64_t *d, int64_t owner, int64_t q, int64_t ep_page, in
   if (!holds_head(P, Hkv, q, h, &hl)) { *ep_off = -1; *tp_off = -1; return; }
   *ep_off = kvslot_at(L, owner, ep_slot, c) + (((ep_page * ps + tok_in_page) * Hkv + h) * D + e) * 2;
   *tp_off = kvslot_at(L, q, tp_slot, c) + (((tp_page * ps + tok_in_page) * L[OL_H_TP] + hl) * D + e) * 2;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention weights (memory-saving variant of §3.1)                          */
+/* ------------------------------------------------------------------------ */
+
+static int64_t attn_at(const int64_t *L, int64_t r, int64_t s) {
+  return r * L[OL_REGION_STRIDE] + L[OL_ATTNSLOTS_OFF] + s * L[OL_ATTN_STRIDE];
+}
+
+/* R-16: the full-layout head held at local head slot b of TP rank q. */
+static int64_t full_head_of(int64_t P, int64_t Hq, int64_t Hkv, int64_t q, int64_t b) {
+  int64_t hq = Hq / P, h_tp = (Hkv >= P) ? Hkv / P : 1;
+  if (b < hq) return q * hq + b;                                  /* query head */
+  int64_t kv = (b - hq) % h_tp, which = (b - hq) / h_tp;         /* 0 = K, 1 = V */
+  int64_t h = (Hkv >= P) ? q * h_tp + kv : q * Hkv / P;
+  return Hq + which * Hkv + h;
+}
+
+/* EP -> TP: every rank keeps its own shard of its own full copy (no rank's
+ * data crosses to another).  Layers ascending: EP slot l+1 -> TP slot l. */
+void orc_attn_ep2tp(const uint8_t *src, uint8_t *dst, const int64_t *d, int order) {
+  int64_t L[OL_COUNT];
+  orc_layout(d, L);
+  int64_t P = d[OD_P], H = d[OD_H], N = d[OD_N], Hkv = d[OD_HKV], D = d[OD_HD], Hq = d[OD_HQ];
+  int64_t hq = Hq / P, h_tp = L[OL_H_TP];
+  for (int64_t t = 0; t < N; ++t) {
+    int64_t l = (order >= 0) ? t : N - 1 - t;
+    for (int64_t q = 0; q < P; ++q) {
+      for (int64_t b = 0; b < hq + 2 * h_tp; ++b) {
+        int64_t hh = full_head_of(P, Hq, Hkv, q, b);
+        for (int64_t i = 0; i < D * H; ++i)
+          copy2(src, dst, attn_at(L, q, l + 1) + (hh * D * H + i) * 2, attn_at(L, q, l) + (b * D * H + i) * 2);
+      }
+      for (int64_t row = 0; row < H; ++row)
+        for (int64_t c = 0; c < hq * D; ++c)
+          copy2(src, dst, attn_at(L, q, l + 1) + L[OL_ATTN_WO_OFF] + (row * Hq * D + q * hq * D + c) * 2,
+                attn_at(L, q, l) + L[OL_ATTN_WO_OFF] + (row * hq * D + c) * 2);
+    }
+  }
+}
+
+/* TP -> EP (all-gather): every rank's full copy is rebuilt from the shards:
+ * query head hh from rank hh / (Hq/P); key or value head h from the lowest
+ * rank holding it (R-4); Wo column j from rank j / ((Hq/P) * Dh).  Layers
+ * descending: TP slot l -> EP slot l+1. */
+void orc_attn_tp2ep(const uint8_t *src, uint8_t *dst, const int64_t *d, int order) {
+  int64_t L[OL_COUNT];
+  orc_layout(d, L);
+  int64_t P = d[OD_P], H = d[OD_H], N = d[OD_N], Hkv = d[OD_HKV], D = d[OD_HD], Hq = d[OD_HQ];
+  int64_t hq = Hq / P, h_tp = L[OL_H_TP];
+  for (int64_t t = 0; t < N; ++t) {
+    int64_t l = (order < 0) ? N - 1 - t : t;
+    for (int64_t r = 0; r < P; ++r) {
+      for (int64_t hh = 0; hh < Hq + 2 * Hkv; ++hh) {
+        int64_t q, b;
+        if (hh < Hq) {
+          q = hh / hq;
+          b = hh % hq;
+        } else {
+          int64_t which = (hh - Hq) / Hkv, h = (hh - Hq) % Hkv, hl = 0;
+          q = 0;
+          while (!holds_head(P, Hkv, q, h, &hl)) ++q;
+          b = hq + which * h_tp + hl;
+        }
+        for (int64_t i = 0; i < D * H; ++i)
+          copy2(src, dst, attn_at(L, q, l) + (b * D * H + i) * 2, attn_at(L, r, l + 1) + (hh * D * H + i) * 2);
+      }
+      for (int64_t row = 0; row < H; ++row)
+        for (int64_t j = 0; j < Hq * D; ++j) {
+          int64_t q = j / (hq * D), c = j % (hq * D);
+          copy2(src, dst, attn_at(L, q, l) + L[OL_ATTN_WO_OFF] + (row * hq * D + c) * 2,
+                attn_at(L, r, l + 1) + L[OL_ATTN_WO_OFF] + (row * Hq * D + j) * 2);
+        }
+    }
+  }
 }
 
 /* ------------------------------------------------------------------------ */

@@ -35,6 +35,7 @@ class Workload:
     kv_sigma: float | None = None
     seed: int = 0
     slack: float = 1.02            # TP page pool = slack * pages in use
+    Hq: int = 0                    # attention query heads (0 = no attention weights)
 
     @property
     def h_tp(self) -> int:
@@ -56,6 +57,8 @@ class Workload:
         rounded up so that the EP view (all heads per page) has whole pages."""
         if self.Hkv == 0:
             return 0
+        if self.R == 0:       # heads without a cache (attention weights only)
+            return self.Hkv // self.h_tp
         used = int(npages(self.lengths(), self.ps).sum())
         n = max(1, math.ceil(self.slack * used))
         m = self.Hkv // self.h_tp
@@ -65,7 +68,7 @@ class Workload:
         ptp = self.pages_tp()
         return dict(P=self.P, E=self.E, H=self.H, I=self.I, N=self.N, Hkv=self.Hkv, D=self.D,
                     ps=self.ps, pages_tp=ptp, max_requests=max(self.R, 1),
-                    max_pages=max(ptp, 1), w13_split=0)
+                    max_pages=max(ptp, 1), w13_split=0, Hq=self.Hq)
 
     def w_mode(self):
         return (RAW, 1.0) if self.w_sigma is None else (NORMAL, self.w_sigma)
@@ -96,5 +99,10 @@ FULL_SWITCH = Workload("full_switch_p8_e128_h2048_i768_8layers_2048req_lognormal
 KV_PROFILE = KV_256REQ.with_(name="kv_p8_2layers_8req_u1k-32k_hkv4_d128", N=2, R=8)
 WEIGHTS_PROFILE = WEIGHTS_H2048.with_(name="weights_p8_e128_h2048_i768_2layers", N=2)
 
+# Attention weights of the page's model shape (64 query / 4 KV heads of 128,
+# hidden 4096), memory-saving variant, 8 layers.
+ATTN_QWEN3_SHAPE = Workload("attn_p8_h4096_hq64_hkv4_d128_8layers", P=8, N=8, H=4096, Hkv=4, D=128, Hq=64,
+                            w_sigma=0.02)
+
 ALL = {w.name: w for w in (TINY, WEIGHTS_H2048, WEIGHTS_H4096, KV_256REQ, FULL_SWITCH, KV_PROFILE,
-                           WEIGHTS_PROFILE)}
+                           WEIGHTS_PROFILE, ATTN_QWEN3_SHAPE)}

@@ -26,7 +26,7 @@ def lib_dims(w: Workload, **over):
                          ps=d["ps"], pages_tp=d["pages_tp"], max_requests=d["max_requests"],
                          max_pages=d["max_pages"], w13_split=d["w13_split"],
                          weight_mode=d.get("weight_mode", umm.UMM_MODE_EP),
-                         kv_mode=d.get("kv_mode", umm.UMM_MODE_EP))
+                         kv_mode=d.get("kv_mode", umm.UMM_MODE_EP), Hq=d.get("Hq", 0))
 
 
 def fill_device(buf: torch.Tensor, L: dict, w: Workload, seed: int, stream=None) -> None:

@@ -147,3 +147,27 @@ def read_golden(name: str) -> list[str]:
 
 def ints(s: str) -> list[int]:
     return [int(x) for x in re.findall(r"-?\d+", s)]
+
+
+# ---- attention weights (memory-saving variant): views of one attention slot
+
+def attnslot(L: dict, r: int, s: int) -> int:
+    return r * L["region_stride"] + L["attnslots_off"] + s * L["attnslot_stride"]
+
+
+def attn_full_qkv(buf, L, d, r, s):
+    """EP view: [Hq + 2*Hkv heads][Dh * H] (each head Dh rows of H)."""
+    return u16(buf, attnslot(L, r, s), (d.Hq + 2 * d.Hkv, d.D * d.H))
+
+
+def attn_full_wo(buf, L, d, r, s):
+    return u16(buf, attnslot(L, r, s) + L["attn_wo_off"], (d.H, d.Hq * d.D))
+
+
+def attn_shard_qkv(buf, L, d, q, s):
+    """TP view of rank q: [Hq/P + 2*h_tp heads][Dh * H]."""
+    return u16(buf, attnslot(L, q, s), (d.Hq // d.P + 2 * L["h_tp"], d.D * d.H))
+
+
+def attn_shard_wo(buf, L, d, q, s):
+    return u16(buf, attnslot(L, q, s) + L["attn_wo_off"], (d.H, d.Hq // d.P * d.D))

@@ -58,8 +58,8 @@ def test_binding_constants_match_header(umm):
 
 
 def test_struct_sizes_match_c_abi(umm):
-    assert ctypes.sizeof(umm.UmmDims) == 64
-    assert ctypes.sizeof(umm.UmmLayout) == 128
+    assert ctypes.sizeof(umm.UmmDims) == 72
+    assert ctypes.sizeof(umm.UmmLayout) == 152
 
 
 def lib_dims(umm, w: Workload, **over):
@@ -67,7 +67,7 @@ def lib_dims(umm, w: Workload, **over):
     d.update(over)
     return umm.make_dims(P=d["P"], E=d["E"], H=d["H"], I=d["I"], N=d["N"], Hkv=d["Hkv"], D=d["D"],
                          ps=d["ps"], pages_tp=d["pages_tp"], max_requests=d["max_requests"],
-                         max_pages=d["max_pages"], w13_split=d["w13_split"])
+                         max_pages=d["max_pages"], w13_split=d["w13_split"], Hq=d.get("Hq", 0))
 
 
 @pytest.mark.parametrize("name", sorted(ALL))

@@ -364,3 +364,39 @@ def test_kv_staged_equals_oracle(w):
     assert dev.status() == (0, 0)
     np.testing.assert_array_equal(dev.host(), ref)
     dev.close()
+
+
+# ------------------------------------------------------------------ attention weights (memory-saving variant)
+
+ATTN_CASES = [
+    Workload("attn_p2_hq2_hkv1", P=2, N=2, H=64, Hkv=1, D=16, Hq=2),
+    Workload("attn_p4_hq8_hkv2", P=4, N=3, H=96, Hkv=2, D=8, Hq=8, w_sigma=0.02),
+    Workload("attn_p4_hq8_hkv8_odd", P=4, N=2, H=36, Hkv=8, D=6, Hq=8),           # 8-byte vectors
+    Workload("attn_p8_hq64_hkv4_d128", P=8, N=2, H=512, Hkv=4, D=128, Hq=64, w_sigma=0.02),
+    Workload("attn_p4_h7", P=4, N=2, H=7, Hkv=4, D=3, Hq=4),                       # 2-byte vectors
+]
+
+
+@pytest.mark.parametrize("w", ATTN_CASES, ids=lambda w: w.name)
+def test_attn_full_buffer_parity(w):
+    dev = DevUMM(w, seed=15)
+    ref = dev.host()
+    umm.reshard_attn_ep2tp(dev.h)
+    oracle.attn_ep2tp(ref, dev.d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    assert umm.umm_get_attn_mode(dev.h) == umm.UMM_MODE_TP
+    with pytest.raises(umm.UmmError) as ei:
+        umm.reshard_attn_ep2tp(dev.h)
+    assert ei.value.code == umm.UMM_ERR_MODE
+    umm.reshard_attn_tp2ep(dev.h)
+    oracle.attn_tp2ep(ref, dev.d)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
+
+
+def test_attn_needs_attention_dims():
+    dev = DevUMM(TINY, seed=1)
+    with pytest.raises(umm.UmmError) as ei:
+        umm.reshard_attn_ep2tp(dev.h)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    dev.close()

@@ -580,3 +580,108 @@ def test_generator_normal_table_and_raw():
     assert len(np.unique(x)) > 40000
     a = synth.fill_host(1000, 5, base=123)
     assert np.array_equal(a, synth.values_at(5, np.arange(123, 1123)))
+
+
+# ----------------------------------------------------------------------------- attention (memory-saving variant)
+
+from helpers import attn_full_qkv, attn_full_wo, attn_shard_qkv, attn_shard_wo  # noqa: E402
+
+ATTN = [Workload("attn_hkv2_p4", P=4, N=2, H=12, Hkv=2, D=4, Hq=8, w_sigma=0.5),
+        Workload("attn_hkv8_p4", P=4, N=2, H=8, Hkv=8, D=2, Hq=4, w_sigma=0.5),
+        Workload("attn_hkv4_p4", P=4, N=3, H=6, Hkv=4, D=3, Hq=12, w_sigma=0.5)]
+
+
+def _attn_setup(w, seed):
+    """EP state: the same full copy on every rank (DP attention replicas)."""
+    d = dims_of(w)
+    L = oracle.layout(d)
+    buf = fill_regions(L, w, seed=seed)
+    for r in range(1, d.P):
+        for s in range(d.N + 1):
+            a = L["attnslots_off"] + s * L["attnslot_stride"]
+            buf[r * L["region_stride"] + a: r * L["region_stride"] + a + L["attnslot_stride"]] = \
+                buf[a:a + L["attnslot_stride"]]
+    return d, L, buf
+
+
+def test_attn_golden_hand_worked():
+    g = read_golden("attn_p2_hq2_hkv1.txt")
+    kv = {ln.split()[0]: int(ln.split()[1]) for ln in g if ln.split()[0] in ("P", "Hq", "Hkv", "D", "H")}
+    d = oracle.Dims(P=kv["P"], H=kv["H"], N=1, Hkv=kv["Hkv"], D=kv["D"], ps=1, pages_tp=1, Hq=kv["Hq"])
+    L = oracle.layout(d)
+    buf = np.zeros(L["ws_off"], dtype=np.uint8)
+    for r in range(d.P):
+        qkv = attn_full_qkv(buf, L, d, r, 1)
+        for hh in range(d.Hq + 2 * d.Hkv):
+            qkv[hh] = 10 * hh + np.arange(d.H)
+        wo = attn_full_wo(buf, L, d, r, 1)
+        for i in range(d.H):
+            wo[i] = 100 + 10 * i + np.arange(d.Hq * d.D)
+    oracle.attn_ep2tp(buf, d)
+    n = 0
+    for ln in g:
+        name, rest = ln.split(" ", 1)
+        if name not in ("shard_qkv", "shard_wo"):
+            continue
+        head, vals = rest.split(":")
+        q = ints(head)[0]
+        got = (attn_shard_qkv if name == "shard_qkv" else attn_shard_wo)(buf, L, d, q, 0).ravel().tolist()
+        assert got == ints(vals), (name, q)
+        n += 1
+    assert n == 4
+
+
+@pytest.mark.parametrize("w", ATTN, ids=lambda w: w.name)
+def test_attn_tp_shards_compute_the_same_projections(w):
+    """§3: the TP shards compute the same function.  Every rank's query/key/
+    value projections equal the full copy's for its heads, and the sum over
+    ranks of their output-projection partials equals the full output
+    projection (the All-Reduce of row-parallel Wo)."""
+    d, L, buf = _attn_setup(w, 3)
+    before = buf.copy()
+    oracle.attn_ep2tp(buf, d)
+    rng = np.random.default_rng(2)
+    hq = d.Hq // d.P
+    for layer in range(d.N):
+        x = rng.normal(size=d.H)
+        u = rng.normal(size=(d.Hq, d.D))
+        full_qkv = bf16_to_f64(attn_full_qkv(before, L, d, 0, layer + 1))
+        full_wo = bf16_to_f64(attn_full_wo(before, L, d, 0, layer + 1))
+        y_full = full_wo @ u.ravel()
+        y_tp = np.zeros(d.H)
+        for q in range(d.P):
+            sq = bf16_to_f64(attn_shard_qkv(buf, L, d, q, layer))
+            heads = list(range(q * hq, (q + 1) * hq))
+            kvh = heads_of_rank(d.P, d.Hkv, q)
+            want = [full_qkv[h] for h in heads] + [full_qkv[d.Hq + h] for h in kvh] + \
+                   [full_qkv[d.Hq + d.Hkv + h] for h in kvh]
+            for b, wrow in enumerate(want):      # one head: Dh rows of H
+                np.testing.assert_array_equal(sq[b].reshape(d.D, d.H) @ x, wrow.reshape(d.D, d.H) @ x)
+            wo_q = bf16_to_f64(attn_shard_wo(buf, L, d, q, layer))
+            y_tp += wo_q @ u[heads].ravel()
+        np.testing.assert_allclose(y_tp, y_full, rtol=1e-9, atol=1e-12)
+
+
+@pytest.mark.parametrize("w", ATTN, ids=lambda w: w.name)
+def test_attn_round_trip_and_layer_order(w):
+    """EP -> TP -> EP restores every rank's full copy (all-gather), the
+    in-place layer orders equal the snapshot definition, and slot N is not a
+    destination of EP->TP."""
+    d, L, orig = _attn_setup(w.with_(w_sigma=None), 5)
+    buf = orig.copy()
+    oracle.attn_ep2tp(buf, d)
+    snap = orig.copy()
+    oracle.attn_ep2tp(snap, d, src=orig.copy())
+    assert np.array_equal(buf, snap)
+    for r in range(d.P):
+        a = r * L["region_stride"] + L["attnslots_off"] + d.N * L["attnslot_stride"]
+        assert np.array_equal(buf[a:a + L["attnslot_stride"]], orig[a:a + L["attnslot_stride"]])
+    mid = buf.copy()
+    oracle.attn_tp2ep(buf, d)
+    snap2 = mid.copy()
+    oracle.attn_tp2ep(snap2, d, src=mid.copy())
+    assert np.array_equal(buf, snap2)
+    for r in range(d.P):
+        a = r * L["region_stride"] + L["attnslots_off"] + L["attnslot_stride"]
+        b = r * L["region_stride"] + L["attnslots_off"] + (d.N + 1) * L["attnslot_stride"]
+        assert np.array_equal(buf[a:b], orig[a:b]), r
