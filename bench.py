@@ -494,12 +494,13 @@ def run_umm(args, rank, world, local_rank):
 
 class CpuSample:
     """The oracle, as it stands, on a bounded sample of the workload: the
-    expert weights of every layer EP->TP->EP, and the KV cache of the first
-    1024 requests for one layer EP->TP->EP (greedy placement, fresh pages).
-    Buffer contents do not change the oracle's speed, so they are left as
-    allocated (zero pages, touched once before timing)."""
+    expert weights of every layer EP->TP->EP, and the KV cache of all requests
+    (at most 2048) for one layer EP->TP->EP, three times (greedy placement,
+    fresh pages each time).  Buffer contents do not change the oracle's speed,
+    so they are left as allocated (touched once before timing)."""
 
-    KV_REQUESTS = 1024
+    KV_REQUESTS = 2048
+    KV_ROUNDS = 3
 
     def __init__(self, w, threads: int):
         import oracle
@@ -548,8 +549,8 @@ class CpuSample:
         if self.wbuf is not None:
             parts.append(f"expert weights of all {self.w.N} layers EP->TP->EP")
         if self.kbuf is not None:
-            parts.append(f"KV of the first {min(self.KV_REQUESTS, self.w.R)} of {self.w.R} requests for 1 layer "
-                         f"EP->TP->EP")
+            parts.append(f"KV of {min(self.KV_REQUESTS, self.w.R)} of {self.w.R} requests for 1 layer "
+                         f"EP->TP->EP, {self.KV_ROUNDS} times")
         return f"plain C oracle (element by element, OpenMP, {self.threads} threads): " + " + ".join(parts)
 
     def run(self):
@@ -568,7 +569,7 @@ class CpuSample:
             o.weights_tp2ep(self.wbuf, self.wd)
             secs += time.perf_counter() - t
             moved += self.wbytes
-        if self.kbuf is not None:
+        for _ in range(self.KV_ROUNDS if self.kbuf is not None else 0):
             L = self.kL
             self.n_runs += 1
             pos = o.request_order(w.P, self.owner)

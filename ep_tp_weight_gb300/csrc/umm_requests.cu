@@ -16,6 +16,8 @@
 
 namespace uk {
 
+constexpr int kMaxDevices = 64;
+
 // ------------------------------------------------------------------ list order (EP -> TP)
 
 __global__ void __launch_bounds__(kScanThreads)
@@ -265,11 +267,17 @@ cudaError_t launch_place(const Geo& g, const Ws& w, int32_t R, const int32_t* le
   const size_t need = (size_t)n2 * sizeof(unsigned long long);
   const int in_smem = need <= 128 * 1024;
   const size_t dyn = in_smem ? need : 0;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  // the shared-memory limit is a per-device function attribute: set it once
+  // per device (calls on one handle come from one host thread)
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   place_kernel<<<1, kScanThreads, dyn, s>>>(g, w, R, lens, list_pos, owner, local_pos, in_smem, call);
   return cudaGetLastError();

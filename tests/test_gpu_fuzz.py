@@ -1,0 +1,113 @@
+"""Randomised parity of the CUDA path with the oracle: random rank counts,
+expert and hidden sizes (including sizes that force 8-, 4- and 2-byte
+vectors), head ratios, page sizes and request mixes (zero lengths, exact
+page multiples, one-token requests), through the fused, staged and
+attention entry points, whole buffers compared, both directions."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import ep_tp_weight_gb300 as umm
+import oracle
+import synth
+from gpu_helpers import DevUMM, i32
+from helpers import dims_of
+from synth.workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+
+def random_case(seed: int):
+    rng = np.random.default_rng(1000 + seed)
+    P = int(rng.choice([1, 2, 3, 4, 6, 8, 16]))
+    N = int(rng.integers(1, 4))
+    E = P * int(rng.integers(1, 4))
+    I = P * int(rng.integers(1, 7))
+    H = int(rng.integers(1, 70))
+    if rng.random() < 0.5:
+        Hkv = P * int(rng.choice([1, 2, 4]))            # Hkv >= P
+    else:
+        divs = [h for h in range(1, P + 1) if P % h == 0]
+        Hkv = int(rng.choice(divs))                      # Hkv <= P, a divisor
+    D = int(rng.integers(1, 20))
+    ps = int(rng.integers(1, 33))
+    R = int(rng.integers(0, 40))
+    Hq = P * int(rng.integers(1, 4)) if rng.random() < 0.6 else 0
+    return rng, Workload(f"fuzz{seed}", P=P, N=N, E=E, H=H, I=I, Hkv=Hkv, D=D, ps=ps, R=max(R, 1),
+                         len_kind="uniform", len_a=0, len_b=int(rng.integers(1, 5 * ps + 2)), slack=1.0 + P,
+                         Hq=Hq), R
+
+
+def pool_pages(w: Workload, R: int) -> int:
+    """A TP pool large enough that every EP rank could hold all live pages."""
+    m = w.Hkv // w.h_tp
+    total = R * ((int(w.len_b) + w.ps - 1) // w.ps) + 1
+    return m * total
+
+
+def kv_state(rng, w: Workload, d, L: dict, R: int):
+    """Random lengths (with zeros and exact multiples), greedy owners, random pages."""
+    lens = rng.integers(0, int(w.len_b) + 1, R).astype(np.int32)
+    if R > 2:
+        lens[0] = 0
+        lens[1] = w.ps * max(1, int(w.len_b) // w.ps)
+    maxp = max(1, int(np.ceil(max(1, int(lens.max()) if R else 1) / w.ps)))
+    owner, _, _ = oracle.place(w.P, lens)
+    free_ep = synth.permutation(int(rng.integers(1 << 30)), 2, L["pages_ep"], rows=w.P)
+    fl, ep_pt = oracle.assign_pages(w.P, lens, w.ps, maxp, free_ep, region=owner)
+    pos = oracle.request_order(w.P, owner)
+    fl2, tp_pt = oracle.assign_pages(1, lens, w.ps, maxp, synth.permutation(int(rng.integers(1 << 30)), 3,
+                                                                             L["pages_tp"]), key=pos)
+    owner2, _, _ = oracle.place(w.P, lens, key=pos)
+    fl3, ep_pt2 = oracle.assign_pages(w.P, lens, w.ps, maxp, synth.permutation(int(rng.integers(1 << 30)), 4,
+                                                                               L["pages_ep"], w.P),
+                                      region=owner2, key=pos)
+    ok = fl == 0 and fl2 == 0 and fl3 == 0
+    return ok, lens, maxp, owner, ep_pt, tp_pt, owner2, ep_pt2
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_parity(seed):
+    rng, w, R = random_case(seed)
+    ptp = pool_pages(w, R)
+    dev = DevUMM(w, seed=seed, pages_tp=ptp, max_requests=R, max_pages=ptp)
+    L, d = dev.L, dev.d
+    staged = bool(seed % 2)
+    ok, lens, maxp, owner, ep_pt, tp_pt, owner2, ep_pt2 = kv_state(rng, w, d, L, R)
+    assert ok
+    ref = dev.host()
+    g = i32
+    stage_w = torch.empty(umm.umm_weights_stage_bytes(dev.h), dtype=torch.uint8, device="cuda")
+    stage_k = torch.empty(umm.umm_kv_stage_bytes(dev.h), dtype=torch.uint8, device="cuda")
+    # EP -> TP
+    if staged:
+        umm.reshard_weights_ep2tp_staged(dev.h, stage_w, stage_w.numel())
+        umm.reshard_kv_ep2tp_staged(dev.h, stage_k, stage_k.numel(), R, maxp, g(lens), g(owner), g(ep_pt), g(tp_pt))
+    else:
+        umm.reshard_weights_ep2tp(dev.h)
+        umm.reshard_kv_ep2tp(dev.h, R, maxp, g(lens), g(owner), g(ep_pt), g(tp_pt))
+    if w.Hq:
+        umm.reshard_attn_ep2tp(dev.h)
+        oracle.attn_ep2tp(ref, d)
+    oracle.weights_ep2tp(ref, d)
+    assert oracle.kv_ep2tp(ref, d, lens, owner, ep_pt, tp_pt) == 0
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    # TP -> EP
+    if staged:
+        umm.reshard_weights_tp2ep_staged(dev.h, stage_w, stage_w.numel())
+        umm.reshard_kv_tp2ep_staged(dev.h, stage_k, stage_k.numel(), R, maxp, g(lens), g(owner2), g(ep_pt2),
+                                    g(tp_pt))
+    else:
+        umm.reshard_weights_tp2ep(dev.h)
+        umm.reshard_kv_tp2ep(dev.h, R, maxp, g(lens), g(owner2), g(ep_pt2), g(tp_pt))
+    if w.Hq:
+        umm.reshard_attn_tp2ep(dev.h)
+        oracle.attn_tp2ep(ref, d)
+    oracle.weights_tp2ep(ref, d)
+    assert oracle.kv_tp2ep(ref, d, lens, owner2, ep_pt2, tp_pt) == 0
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
