@@ -386,7 +386,7 @@ def run_umm(args, rank, world, local_rank):
 
     # ---------------- the staged (collective-style) path, same steps, for comparison
     staged = None
-    if not args.no_staged:
+    if not args.no_staged and (w.E or have_kv):
         wsb = umm.umm_weights_stage_bytes(h) if w.E else 0
         ksb = umm.umm_kv_stage_bytes(h) if have_kv else 0
         wsb_al = (wsb + 255) // 256 * 256
