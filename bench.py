@@ -282,33 +282,28 @@ def run_umm(args, rank, world, local_rank):
     ev_half = []
 
     def step(mark=False):
+        """One round trip: umm_switch_ep2tp then umm_switch_tp2ep (weights,
+        attention, request order, pages, KV; the state moves to the new EP
+        owners and pages)."""
         e0 = torch.cuda.Event(enable_timing=True) if mark else None
         if mark:
             e0.record(s)
-        if w.Hq:
-            umm.reshard_attn_ep2tp(h, s)
-        if w.E:
-            umm.reshard_weights_ep2tp(h, s)
         if have_kv:
-            umm.gather_requests_ep2tp(h, R, state["owner"], tp_pos, s)
-            umm.umm_assign_pages(h, 1, R, lens, None, tp_pos, tp_free, L["pages_tp"], L["pages_tp"], tp_pt, maxp, s)
-            umm.reshard_kv_ep2tp(h, R, maxp, lens, state["owner"], state["ep_pt"], tp_pt, s)
+            umm.umm_switch_ep2tp(h, R, maxp, lens, state["owner"], state["ep_pt"], tp_free, L["pages_tp"], tp_pos,
+                                 tp_pt, s)
+        else:
+            umm.umm_switch_ep2tp(h, 0, 1, None, None, None, None, 0, None, None, s)
         e1 = None
         if mark:
             e1 = torch.cuda.Event(enable_timing=True)
             e1.record(s)
         if have_kv:
-            umm.place_requests_tp2ep(h, R, lens, tp_pos, state["owner_n"], local, s)
-            umm.umm_assign_pages(h, P, R, lens, state["owner_n"], tp_pos, ep_free, L["pages_ep"], L["pages_ep"],
-                                 state["ep_pt_n"], maxp, s)
-        if w.E:
-            umm.reshard_weights_tp2ep(h, s)
-        if w.Hq:
-            umm.reshard_attn_tp2ep(h, s)
-        if have_kv:
-            umm.reshard_kv_tp2ep(h, R, maxp, lens, state["owner_n"], state["ep_pt_n"], tp_pt, s)
+            umm.umm_switch_tp2ep(h, R, maxp, lens, tp_pos, tp_pt, ep_free, L["pages_ep"], L["pages_ep"],
+                                 state["owner_n"], local, state["ep_pt_n"], s)
             state["owner"], state["owner_n"] = state["owner_n"], state["owner"]
             state["ep_pt"], state["ep_pt_n"] = state["ep_pt_n"], state["ep_pt"]
+        else:
+            umm.umm_switch_tp2ep(h, 0, 1, None, None, None, None, 0, 0, None, None, None, s)
         if mark:
             e2 = torch.cuda.Event(enable_timing=True)
             e2.record(s)

@@ -113,6 +113,8 @@ _SIG = {
     "reshard_attn_tp2ep": [_vp, _vp],
     "umm_get_attn_mode": [_vp, _P(_i32)],
     "umm_set_attn_mode": [_vp, _i32],
+    "umm_switch_ep2tp": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
+    "umm_switch_tp2ep": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp],
     "umm_policy_create": [_vp, _P(_vp)],
     "umm_policy_destroy": [_vp],
     "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
@@ -297,6 +299,21 @@ def reshard_kv_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner,
                      tp_page_table, stream=None) -> None:
     _ck(_lib.reshard_kv_tp2ep(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
                               _ptr(tp_page_table), _stream(stream)), "reshard_kv_tp2ep")
+
+
+def umm_switch_ep2tp(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner, ep_page_table, tp_free_pages,
+                     tp_free_count: int, tp_pos, tp_page_table, stream=None) -> None:
+    _ck(_lib.umm_switch_ep2tp(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
+                              _ptr(tp_free_pages), int(tp_free_count), _ptr(tp_pos), _ptr(tp_page_table),
+                              _stream(stream)), "umm_switch_ep2tp")
+
+
+def umm_switch_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, tp_pos, tp_page_table, ep_free_pages,
+                     ep_free_stride: int, ep_free_count: int, ep_owner, local_pos, ep_page_table,
+                     stream=None) -> None:
+    _ck(_lib.umm_switch_tp2ep(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(tp_pos), _ptr(tp_page_table),
+                              _ptr(ep_free_pages), int(ep_free_stride), int(ep_free_count), _ptr(ep_owner),
+                              _ptr(local_pos), _ptr(ep_page_table), _stream(stream)), "umm_switch_tp2ep")
 
 
 def umm_kv_check_capacity(h: int, target_kv_mode: int, R: int, h_seq_lens, h_ep_owner=None) -> int:

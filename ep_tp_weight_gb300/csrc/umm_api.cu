@@ -428,7 +428,7 @@ int umm_set_modes(umm_t* u, int32_t weight_mode, int32_t kv_mode) {
   return UMM_OK;
 }
 
-int reshard_attn(umm_t* u, int ep2tp, void* stream) {
+static int reshard_attn(umm_t* u, int ep2tp, void* stream) {
   if (!u || u->dims.attn_q_heads == 0) return UMM_ERR_INVALID_ARG;
   if (u->attn_mode != (ep2tp ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
   cudaStream_t s = as_stream(stream);
@@ -551,6 +551,62 @@ int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
                      const int32_t* d_tp_page_table, void* stream) {
   return reshard_kv(u, 1, R, max_pages_per_req, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table,
                     stream);
+}
+
+int umm_switch_ep2tp(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_lens, const int32_t* d_ep_owner,
+                     const int32_t* d_ep_page_table, const int32_t* d_tp_free_pages, int64_t tp_free_count,
+                     int32_t* d_tp_pos, int32_t* d_tp_page_table, void* stream) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  const bool w = u->dims.E > 0, a = u->dims.attn_q_heads > 0, kv = u->dims.num_kv_heads > 0;
+  // every check that can fail on the host runs before anything is enqueued
+  if (w && u->weight_mode != UMM_MODE_EP) return UMM_ERR_MODE;
+  if (a && u->attn_mode != UMM_MODE_EP) return UMM_ERR_MODE;
+  if (kv) {
+    if (u->kv_mode != UMM_MODE_EP) return UMM_ERR_MODE;
+    int rc = check_kv_args(u, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table);
+    if (rc) return rc;
+    if (R > 0 && (!d_tp_free_pages || !d_tp_pos || tp_free_count < 0)) return UMM_ERR_INVALID_ARG;
+  }
+  int rc = UMM_OK;
+  if (w && (rc = reshard_weights(u, 1, stream))) return rc;
+  if (a && (rc = reshard_attn(u, 1, stream))) return rc;
+  if (!kv) return UMM_OK;
+  if (R > 0) {
+    if ((rc = gather_requests_ep2tp(u, R, d_ep_owner, d_tp_pos, stream))) return rc;
+    if ((rc = umm_assign_pages(u, 1, R, d_seq_lens, nullptr, d_tp_pos, d_tp_free_pages, tp_free_count,
+                               tp_free_count, d_tp_page_table, maxp, stream)))
+      return rc;
+  }
+  return reshard_kv(u, 0, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream);
+}
+
+int umm_switch_tp2ep(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_lens, const int32_t* d_tp_pos,
+                     const int32_t* d_tp_page_table, const int32_t* d_ep_free_pages, int64_t ep_free_stride,
+                     int64_t ep_free_count, int32_t* d_ep_owner, int32_t* d_local_pos, int32_t* d_ep_page_table,
+                     void* stream) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  const bool w = u->dims.E > 0, a = u->dims.attn_q_heads > 0, kv = u->dims.num_kv_heads > 0;
+  if (w && u->weight_mode != UMM_MODE_TP) return UMM_ERR_MODE;
+  if (a && u->attn_mode != UMM_MODE_TP) return UMM_ERR_MODE;
+  if (kv) {
+    if (u->kv_mode != UMM_MODE_TP) return UMM_ERR_MODE;
+    int rc = check_kv_args(u, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table);
+    if (rc) return rc;
+    if (R > 0 && (!d_ep_free_pages || !d_local_pos || ep_free_count < 0 ||
+                  (u->dims.P > 1 && ep_free_stride < ep_free_count)))
+      return UMM_ERR_INVALID_ARG;
+  }
+  int rc = UMM_OK;
+  if (kv && R > 0) {
+    if ((rc = place_requests_tp2ep(u, R, d_seq_lens, d_tp_pos, d_ep_owner, d_local_pos, stream))) return rc;
+    if ((rc = umm_assign_pages(u, u->dims.P, R, d_seq_lens, d_ep_owner, d_tp_pos, d_ep_free_pages, ep_free_stride,
+                               ep_free_count, d_ep_page_table, maxp, stream)))
+      return rc;
+  }
+  if (w && (rc = reshard_weights(u, 0, stream))) return rc;
+  if (a && (rc = reshard_attn(u, 0, stream))) return rc;
+  if (!kv) return UMM_OK;
+  return reshard_kv(u, 1, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream);
 }
 
 int umm_kv_check_capacity(const umm_t* u, int32_t target_kv_mode, int32_t R, const int32_t* h_seq_lens,

@@ -309,6 +309,28 @@ int reshard_kv_tp2ep_staged(umm_t* u, void* d_stage, uint64_t stage_bytes, int32
                             const int32_t* d_seq_lens, const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
                             const int32_t* d_tp_page_table, void* stream);
 
+/* One whole switch, one call per direction (the "switch between decode
+ * steps" of §3.2 / §4.1): the expert weights (when E > 0), the attention
+ * weights (when attn_q_heads > 0) and, when the KV cache exists, the request
+ * bookkeeping and the KV reshard, all enqueued on `stream` in this order.
+ *
+ * umm_switch_ep2tp: weights, attention, gather_requests_ep2tp (-> d_tp_pos),
+ *   TP pages from d_tp_free_pages in list order (umm_assign_pages, one pool
+ *   -> d_tp_page_table), reshard_kv_ep2tp.
+ * umm_switch_tp2ep: place_requests_tp2ep (list positions d_tp_pos ->
+ *   d_ep_owner, d_local_pos), EP pages from each owner's free list
+ *   (d_ep_free_pages[g*ep_free_stride ..] -> d_ep_page_table), weights,
+ *   attention, reshard_kv_tp2ep.
+ * Host-detectable errors (modes, arguments) are found before anything is
+ * enqueued; device-detected ones follow umm_status_sync(). */
+int umm_switch_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
+                     const int32_t* d_ep_owner, const int32_t* d_ep_page_table, const int32_t* d_tp_free_pages,
+                     int64_t tp_free_count, int32_t* d_tp_pos, int32_t* d_tp_page_table, void* stream);
+int umm_switch_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
+                     const int32_t* d_tp_pos, const int32_t* d_tp_page_table, const int32_t* d_ep_free_pages,
+                     int64_t ep_free_stride, int64_t ep_free_count, int32_t* d_ep_owner, int32_t* d_local_pos,
+                     int32_t* d_ep_page_table, void* stream);
+
 /* §4.5 capacity check on the host, before committing a switch: UMM_OK if the
  * target layout's KV pools hold the requests (TP: all pages in one pool of
  * pages_tp; EP: each owner's pages within pages_ep), else UMM_ERR_CAPACITY.

@@ -43,6 +43,17 @@ def test_library_exports_every_declared_entry_point(umm):
     assert set(names) == set(umm.EXPORTED)
 
 
+def test_library_exports_nothing_undeclared(umm):
+    import shutil
+    import subprocess
+    if not shutil.which("nm"):
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", umm.LIB_PATH], capture_output=True, text=True).stdout
+    c_symbols = {ln.split()[-1] for ln in out.splitlines()
+                 if " T " in ln and not ln.split()[-1].startswith(("_Z", "cuda", "__", "_"))}
+    assert c_symbols == set(declared_functions())
+
+
 def test_binding_constants_match_header(umm):
     d = header_defines()
     for k, v in d.items():

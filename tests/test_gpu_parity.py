@@ -400,3 +400,53 @@ def test_attn_needs_attention_dims():
         umm.reshard_attn_ep2tp(dev.h)
     assert ei.value.code == umm.UMM_ERR_INVALID_ARG
     dev.close()
+
+
+# ------------------------------------------------------------------ one call per direction
+
+@pytest.mark.parametrize("w", [TINY.with_(Hq=4), Workload("switch_mid", P=4, N=3, E=8, H=40, I=24, Hkv=2, D=8, ps=4,
+                                                            R=20, len_a=1, len_b=37, slack=3.0, Hq=8)],
+                         ids=lambda w: w.name)
+def test_switch_entry_points_equal_oracle(w):
+    """umm_switch_ep2tp / umm_switch_tp2ep: weights, attention, request
+    order, page hand-out and KV in one call each; the same bytes and metadata
+    as the oracle's step-by-step definition."""
+    dev = DevUMM(w, seed=17)
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=3)
+    R, maxp = len(st.lens), st.ep_pt.shape[1]
+    ref = dev.host()
+    tp_free = synth.permutation(5, 3, L["pages_tp"], rows=1)
+    ep_free = synth.permutation(5, 4, L["pages_ep"], rows=d.P)
+    d_pos = torch.empty(R, dtype=torch.int32, device="cuda")
+    d_tp_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
+    umm.umm_switch_ep2tp(dev.h, R, maxp, i32(st.lens), i32(st.owner), i32(st.ep_pt), i32(tp_free), L["pages_tp"],
+                         d_pos, d_tp_pt)
+    pos = oracle.request_order(d.P, st.owner)
+    _, tp_pt = oracle.assign_pages(1, st.lens, d.ps, maxp, tp_free, key=pos)
+    oracle.weights_ep2tp(ref, d)
+    oracle.attn_ep2tp(ref, d)
+    assert oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, tp_pt) == 0
+    assert dev.status() == (0, 0)
+    assert np.array_equal(d_pos.cpu().numpy(), pos) and np.array_equal(d_tp_pt.cpu().numpy(), tp_pt)
+    np.testing.assert_array_equal(dev.host(), ref)
+    assert umm.umm_get_modes(dev.h) == (umm.UMM_MODE_TP, umm.UMM_MODE_TP)
+    d_owner = torch.empty(R, dtype=torch.int32, device="cuda")
+    d_local = torch.empty_like(d_owner)
+    d_ep_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
+    umm.umm_switch_tp2ep(dev.h, R, maxp, i32(st.lens), d_pos, d_tp_pt, i32(ep_free), L["pages_ep"], L["pages_ep"],
+                         d_owner, d_local, d_ep_pt)
+    owner2, local2, _ = oracle.place(d.P, st.lens, key=pos)
+    _, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, maxp, ep_free, region=owner2, key=pos)
+    oracle.weights_tp2ep(ref, d)
+    oracle.attn_tp2ep(ref, d)
+    assert oracle.kv_tp2ep(ref, d, st.lens, owner2, ep_pt2, tp_pt) == 0
+    assert dev.status() == (0, 0)
+    assert np.array_equal(d_owner.cpu().numpy(), owner2) and np.array_equal(d_local.cpu().numpy(), local2)
+    assert np.array_equal(d_ep_pt.cpu().numpy(), ep_pt2)
+    np.testing.assert_array_equal(dev.host(), ref)
+    with pytest.raises(umm.UmmError) as ei:      # already EP: nothing enqueued
+        umm.umm_switch_tp2ep(dev.h, R, maxp, i32(st.lens), d_pos, d_tp_pt, i32(ep_free), L["pages_ep"],
+                             L["pages_ep"], d_owner, d_local, d_ep_pt)
+    assert ei.value.code == umm.UMM_ERR_MODE
+    dev.close()
