@@ -173,8 +173,14 @@ PROFILE_CASES = {"kv_copy_ep2tp": "kv_p8_2layers_8req_u1k-32k_hkv4_d128",
 
 
 def source_digest(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 (16 hex) of a source file's code: comments and whitespace are
+    dropped, so edits to comments keep a profile valid and code edits do not."""
+    with open(os.path.join(ROOT, rel)) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
 def committed_traffic(kernel: str, units: dict):

@@ -10,9 +10,10 @@
 //
 // One switch = one descriptor pass (kv_prep_scan: validation, capacity,
 // offsets; kv_prep_emit: one descriptor per live (request, page), page-id
-// checks with warp ballots and a destination bitmap) + one gather/scatter
-// launch per layer (kv_copy).  Nothing is written to the cache unless the
-// descriptor pass raised no flag.
+// checks with warp ballots and destination bitmaps, and an index of the
+// descriptors by TP page) + one gather/scatter launch per layer (kv_copy_*:
+// one CTA per TP page, or per descriptor when the pool is sparsely used).
+// Nothing is written to the cache unless the descriptor pass raised no flag.
 #include <algorithm>
 
 #include "umm_scan.cuh"

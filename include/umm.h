@@ -45,6 +45,8 @@
  *    order, page hand-out) then does nothing until umm_status_sync() reads and
  *    clears them.  Weight reshards cannot fail on the device and ignore them.
  *  - The library never aborts, traps or throws across this ABI.
+ *  - A handle is not thread-safe: issue its calls from one host thread, with
+ *    the buffer's device current.
  */
 #ifndef UMM_H_
 #define UMM_H_

@@ -450,3 +450,34 @@ def test_switch_entry_points_equal_oracle(w):
                              L["pages_ep"], d_owner, d_local, d_ep_pt)
     assert ei.value.code == umm.UMM_ERR_MODE
     dev.close()
+
+
+def test_request_metadata_errors_are_refused_on_device():
+    """Bad owners, pools, list positions and pool shortage raise flags and
+    leave the outputs untouched."""
+    w = Workload("meta_err", P=4, N=1, Hkv=4, D=8, ps=4, R=6, len_a=1, len_b=9)
+    dev = DevUMM(w, fill=False, pages_tp=64, max_requests=8, max_pages=64)
+    lens = i32([3, 9, 1, 4, 8, 2])
+    out = torch.full((6,), -7, dtype=torch.int32, device="cuda")
+    umm.gather_requests_ep2tp(dev.h, 6, i32([0, 1, 4, 2, 3, 1]), out)          # owner 4 >= P
+    assert dev.status()[0] == umm.UMM_ERR_BAD_REQUEST and (out.cpu() == -7).all()
+    own = torch.full((6,), -7, dtype=torch.int32, device="cuda")
+    loc = torch.full((6,), -7, dtype=torch.int32, device="cuda")
+    umm.place_requests_tp2ep(dev.h, 6, lens, i32([0, 1, 2, 2, 4, 5]), own, loc)  # position 2 twice
+    assert dev.status()[0] == umm.UMM_ERR_BAD_REQUEST
+    assert (own.cpu() == -7).all() and (loc.cpu() == -7).all()
+    umm.place_requests_tp2ep(dev.h, 6, i32([3, -1, 1, 4, 8, 2]), None, own, loc)  # negative length
+    assert dev.status()[0] == umm.UMM_ERR_BAD_REQUEST and (own.cpu() == -7).all()
+    pt = torch.full((6, 3), -7, dtype=torch.int32, device="cuda")
+    free = i32(np.arange(40))
+    umm.umm_assign_pages(dev.h, 2, 6, lens, i32([0, 1, 2, 0, 1, 0]), None, free, 20, 20, pt, 3)   # pool 2 >= 2
+    assert dev.status()[0] == umm.UMM_ERR_BAD_REQUEST and (pt.cpu() == -7).all()
+    umm.umm_assign_pages(dev.h, 1, 6, lens, None, i32([5, 4, 3, 2, 1, 7]), free, 40, 40, pt, 3)  # key 7 >= R
+    assert dev.status()[0] == umm.UMM_ERR_BAD_REQUEST and (pt.cpu() == -7).all()
+    umm.umm_assign_pages(dev.h, 1, 6, lens, None, None, free, 40, 8, pt, 3)      # 9 pages needed, 8 free
+    assert dev.status()[0] == umm.UMM_ERR_CAPACITY and (pt.cpu() == -7).all()
+    umm.umm_assign_pages(dev.h, 1, 6, lens, None, None, free, 40, 9, pt, 3)      # exactly enough
+    assert dev.status() == (0, 0)
+    fl, want = oracle.assign_pages(1, [3, 9, 1, 4, 8, 2], 4, 3, np.arange(9))
+    assert fl == 0 and np.array_equal(pt.cpu().numpy(), want)
+    dev.close()
