@@ -161,6 +161,37 @@ def test_order_place_assign_parity(P, R):
     dev.close()
 
 
+# (P, R, length range): together they reach every variant of the device
+# greedy (8 or 16 ranks with 32-bit loads, 16 ranks with 64-bit loads, one
+# rank per lane, loads in local memory) and every sort (registers with 1, 2
+# and 4 keys per thread, the network in shared memory, the network over the
+# workspace).  Totals of 2^27..2^29 tokens and more force the wide words.
+PLACE_VARIANTS = [
+    (8, 1000, (1, 4000)), (8, 4000, (1, 4000)), (7, 9000, (1, 4000)), (8, 17000, (1, 300)),
+    (12, 2500, (1, 4000)), (12, 3000, (100_000, 200_000)), (6, 3000, (150_000, 250_000)),
+    (24, 1500, (1, 4000)), (24, 1500, (100_000, 200_000)), (40, 800, (1, 4000)),
+]
+
+
+@pytest.mark.parametrize("P,R,lr", PLACE_VARIANTS, ids=lambda v: str(v))
+def test_place_variants(P, R, lr):
+    rng = np.random.default_rng(P * 7919 + R)
+    lens = rng.integers(lr[0], lr[1] + 1, R).astype(np.int32)
+    lens[rng.integers(0, R, R // 8)] = lr[0]              # ties on length
+    w = Workload("meta", P=P, N=1, Hkv=P, D=8, ps=16, R=R, len_a=1, len_b=1)
+    dev = DevUMM(w, fill=False, pages_tp=2 * P, max_requests=R, max_pages=2 * P)
+    key = rng.permutation(R).astype(np.int32)
+    owner = torch.empty(R, dtype=torch.int32, device="cuda")
+    local = torch.empty_like(owner)
+    for k in (None, key):
+        umm.place_requests_tp2ep(dev.h, R, i32(lens), None if k is None else i32(k), owner, local)
+        wo, wl, _ = oracle.place(P, lens, k)
+        assert np.array_equal(owner.cpu().numpy(), wo)
+        assert np.array_equal(local.cpu().numpy(), wl)
+    assert dev.status() == (0, 0)
+    dev.close()
+
+
 def test_empty_and_degenerate_requests():
     w = Workload("deg", P=4, N=2, Hkv=4, D=8, ps=4, R=3, len_a=0, len_b=0)
     dev = DevUMM(w, seed=1, pages_tp=8, max_requests=8, max_pages=8)
