@@ -104,5 +104,12 @@ WEIGHTS_PROFILE = WEIGHTS_H2048.with_(name="weights_p8_e128_h2048_i768_2layers",
 ATTN_QWEN3_SHAPE = Workload("attn_p8_h4096_hq64_hkv4_d128_8layers", P=8, N=8, H=4096, Hkv=4, D=128, Hq=64,
                             w_sigma=0.02)
 
+# Small cases for ncu captures of the attention kernel (one layer of the shape
+# above, 2.3 GB on the device) and of the request-metadata kernels (placement,
+# page hand-out, descriptor pass: 2048 requests of 1..64 tokens, one layer).
+ATTN_PROFILE = ATTN_QWEN3_SHAPE.with_(name="attn_p8_h4096_hq64_hkv4_d128_1layer", N=1)
+META_PROFILE = Workload("meta_p8_1layer_2048req_u1-64_hkv4_d128", P=8, N=1, Hkv=4, D=128, ps=16, R=2048,
+                        len_kind="uniform", len_a=1, len_b=64, kv_sigma=1.0)
+
 ALL = {w.name: w for w in (TINY, WEIGHTS_H2048, WEIGHTS_H4096, KV_256REQ, FULL_SWITCH, KV_PROFILE,
-                           WEIGHTS_PROFILE, ATTN_QWEN3_SHAPE)}
+                           WEIGHTS_PROFILE, ATTN_QWEN3_SHAPE, ATTN_PROFILE, META_PROFILE)}

@@ -16,7 +16,8 @@ import ep_tp_weight_gb300 as umm
 import oracle
 import synth
 from gpu_helpers import DevUMM, i32
-from synth.workloads import FULL_SWITCH, KV_256REQ, TINY, WEIGHTS_H2048, WEIGHTS_H4096
+from helpers import attnslot, heads_of_rank
+from synth.workloads import ATTN_QWEN3_SHAPE, FULL_SWITCH, KV_256REQ, TINY, WEIGHTS_H2048, WEIGHTS_H4096
 
 pytestmark = pytest.mark.gpu
 
@@ -105,7 +106,7 @@ def _check_weights_round_trip(dev: DevUMM):
 def test_weights_fullsize(w):
     dev = DevUMM(w, seed=21)
     rng = np.random.default_rng(0)
-    umm.reshard_weights_ep2tp(dev.h)
+    umm.umm_switch_ep2tp(dev.h, 0, 1, None, None, None, None, 0, None, None)    # as bench.py, no requests
     torch.cuda.synchronize()
     _check_weights_ep2tp(dev, rng)
     # slot N is not a destination of EP->TP: untouched
@@ -114,7 +115,7 @@ def test_weights_fullsize(w):
         base = r * L["region_stride"] + w.N * L["wslot_stride"]
         assert torch.equal(dev.u16()[base // 2:(base + L["wslot_stride"]) // 2],
                            _regen(dev, base, L["wslot_stride"], False))
-    umm.reshard_weights_tp2ep(dev.h)
+    umm.umm_switch_tp2ep(dev.h, 0, 1, None, None, None, None, 0, 0, None, None, None)
     torch.cuda.synchronize()
     _check_weights_round_trip(dev)
     dev.close()
@@ -143,31 +144,41 @@ class KVRun:
         _, self.ep_pt1 = oracle.assign_pages(P, self.lens, w.ps, self.maxp, self.ep_free, region=self.owner1,
                                              key=self.pos)
 
-    def ep2tp(self):
+    def ep2tp(self, switch: bool = False):
+        """switch=True: one umm_switch_ep2tp call (weights and attention too),
+        exactly as bench.py times it; else the separate KV entry points."""
         dev, R, maxp = self.dev, self.R, self.maxp
         h, L = dev.h, dev.L
         self.d_lens = i32(self.lens)
         self.d_owner0 = i32(self.owner0)
         self.d_tp_pos = torch.empty(R, dtype=torch.int32, device="cuda")
         self.d_tp_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
-        umm.gather_requests_ep2tp(h, R, self.d_owner0, self.d_tp_pos)
-        umm.umm_assign_pages(h, 1, R, self.d_lens, None, self.d_tp_pos, i32(self.tp_free), L["pages_tp"],
-                             L["pages_tp"], self.d_tp_pt, maxp)
-        umm.reshard_kv_ep2tp(h, R, maxp, self.d_lens, self.d_owner0, i32(self.ep_pt0), self.d_tp_pt)
+        if switch:
+            umm.umm_switch_ep2tp(h, R, maxp, self.d_lens, self.d_owner0, i32(self.ep_pt0), i32(self.tp_free),
+                                 L["pages_tp"], self.d_tp_pos, self.d_tp_pt)
+        else:
+            umm.gather_requests_ep2tp(h, R, self.d_owner0, self.d_tp_pos)
+            umm.umm_assign_pages(h, 1, R, self.d_lens, None, self.d_tp_pos, i32(self.tp_free), L["pages_tp"],
+                                 L["pages_tp"], self.d_tp_pt, maxp)
+            umm.reshard_kv_ep2tp(h, R, maxp, self.d_lens, self.d_owner0, i32(self.ep_pt0), self.d_tp_pt)
         assert dev.status() == (0, 0)
         assert np.array_equal(self.d_tp_pos.cpu().numpy(), self.pos)
         assert np.array_equal(self.d_tp_pt.cpu().numpy(), self.tp_pt)
 
-    def tp2ep(self):
+    def tp2ep(self, switch: bool = False):
         dev, R, maxp = self.dev, self.R, self.maxp
         h, L, P = dev.h, dev.L, dev.w.P
         o1 = torch.empty(R, dtype=torch.int32, device="cuda")
         l1 = torch.empty_like(o1)
         pt1 = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
-        umm.place_requests_tp2ep(h, R, self.d_lens, self.d_tp_pos, o1, l1)
-        umm.umm_assign_pages(h, P, R, self.d_lens, o1, self.d_tp_pos, i32(self.ep_free), L["pages_ep"],
-                             L["pages_ep"], pt1, maxp)
-        umm.reshard_kv_tp2ep(h, R, maxp, self.d_lens, o1, pt1, self.d_tp_pt)
+        if switch:
+            umm.umm_switch_tp2ep(h, R, maxp, self.d_lens, self.d_tp_pos, self.d_tp_pt, i32(self.ep_free),
+                                 L["pages_ep"], L["pages_ep"], o1, l1, pt1)
+        else:
+            umm.place_requests_tp2ep(h, R, self.d_lens, self.d_tp_pos, o1, l1)
+            umm.umm_assign_pages(h, P, R, self.d_lens, o1, self.d_tp_pos, i32(self.ep_free), L["pages_ep"],
+                                 L["pages_ep"], pt1, maxp)
+            umm.reshard_kv_tp2ep(h, R, maxp, self.d_lens, o1, pt1, self.d_tp_pt)
         assert dev.status() == (0, 0)
         assert np.array_equal(o1.cpu().numpy(), self.owner1)
         assert np.array_equal(l1.cpu().numpy(), self.local1)
@@ -270,24 +281,93 @@ def _check_kv_untouched(run: KVRun, rng):
 
 @pytest.mark.parametrize("w", [KV_256REQ, FULL_SWITCH], ids=lambda w: w.name)
 def test_kv_and_full_switch_fullsize(w):
+    """KV alone through the separate entry points; the full switch through
+    umm_switch_ep2tp / umm_switch_tp2ep, the calls bench.py times."""
     dev = DevUMM(w, seed=w.seed)
     run = KVRun(dev)
     rng = np.random.default_rng(1)
-    if w.E:
-        umm.reshard_weights_ep2tp(dev.h)
-    run.ep2tp()
+    switch = bool(w.E)
+    run.ep2tp(switch)
     torch.cuda.synchronize()
     _check_kv_ep2tp(run, rng)
     _check_kv_whole_requests(run, [int(np.argmax(run.lens)), int(np.argmin(run.lens)), 0])
     _check_kv_untouched(run, rng)
     if w.E:
         _check_weights_ep2tp(dev, rng)
-        umm.reshard_weights_tp2ep(dev.h)
-    run.tp2ep()
+    run.tp2ep(switch)
     torch.cuda.synchronize()
     _check_kv_tp2ep(run, rng)
     if w.E:
         _check_weights_round_trip(dev)
+    dev.close()
+
+
+def _attn_views(dev: DevUMM, r: int, slot: int, full: bool):
+    """(QKV heads, Wo) of one attention slot as device tensors: EP (full) or
+    TP (shard) view, the shapes of §3.1's attention part."""
+    w, L = dev.w, dev.L
+    base = attnslot(L, r, slot) // 2
+    nh = w.Hq + 2 * w.Hkv if full else w.Hq // w.P + 2 * L["h_tp"]
+    ncol = w.Hq * w.D if full else w.Hq // w.P * w.D
+    u = dev.u16()
+    qkv = u[base:base + nh * w.D * w.H].view(nh, w.D * w.H)
+    wo_at = base + L["attn_wo_off"] // 2
+    return qkv, u[wo_at:wo_at + w.H * ncol].view(w.H, ncol)
+
+
+def _attn_initial(dev: DevUMM, r: int, slot: int):
+    w, L = dev.w, dev.L
+    nh = w.Hq + 2 * w.Hkv
+    off = attnslot(L, r, slot)
+    qkv = _regen(dev, off, 2 * nh * w.D * w.H, False).view(nh, w.D * w.H)
+    wo = _regen(dev, off + L["attn_wo_off"], 2 * w.H * w.Hq * w.D, False).view(w.H, w.Hq * w.D)
+    return qkv, wo
+
+
+def test_attn_fullsize():
+    """Attention weights of the page's model shape (64 query / 4 KV heads of
+    128, hidden 4096, 8 layers) through umm_switch_*: every TP shard equals the
+    torch slice of its own rank's full copy (memory-saving variant: EP->TP is a
+    local extraction), and after TP->EP every rank holds the all-gather of the
+    shards (KV heads from the lowest rank holding them)."""
+    w = ATTN_QWEN3_SHAPE
+    dev = DevUMM(w, seed=5)
+    P, Hq, Hkv, D = w.P, w.Hq, w.Hkv, w.D
+    qh = Hq // P
+    umm.umm_switch_ep2tp(dev.h, 0, 1, None, None, None, None, 0, None, None)
+    torch.cuda.synchronize()
+    assert umm.umm_get_attn_mode(dev.h) == umm.UMM_MODE_TP
+    for layer in range(w.N):
+        for q in range(P):
+            full, wo = _attn_initial(dev, q, layer + 1)
+            kvh = heads_of_rank(P, Hkv, q)
+            want = torch.cat([full[q * qh:(q + 1) * qh], full[[Hq + h for h in kvh]],
+                              full[[Hq + Hkv + h for h in kvh]]])
+            got_qkv, got_wo = _attn_views(dev, q, layer, full=False)
+            assert torch.equal(got_qkv, want), (layer, q)
+            assert torch.equal(got_wo, wo[:, q * qh * D:(q + 1) * qh * D]), (layer, q)
+    # expected full copies after TP->EP, from the shards now in the TP slots
+    want_full = []
+    for layer in range(w.N):
+        shards = [_attn_views(dev, q, layer, full=False) for q in range(P)]
+        lowest = {}
+        for q in range(P):
+            for i, h in enumerate(heads_of_rank(P, Hkv, q)):
+                lowest.setdefault(h, (q, i))
+        h_tp = len(heads_of_rank(P, Hkv, 0))
+        k_rows = [shards[lowest[h][0]][0][qh + lowest[h][1]] for h in range(Hkv)]
+        v_rows = [shards[lowest[h][0]][0][qh + h_tp + lowest[h][1]] for h in range(Hkv)]
+        qkv = torch.cat([torch.cat([s[0][:qh] for s in shards]), torch.stack(k_rows), torch.stack(v_rows)])
+        wo = torch.cat([s[1] for s in shards], dim=1)
+        want_full.append((qkv.clone(), wo.clone()))
+    umm.umm_switch_tp2ep(dev.h, 0, 1, None, None, None, None, 0, 0, None, None, None)
+    torch.cuda.synchronize()
+    assert umm.umm_get_attn_mode(dev.h) == umm.UMM_MODE_EP
+    for layer in range(w.N):
+        for r in range(P):
+            got_qkv, got_wo = _attn_views(dev, r, layer + 1, full=True)
+            assert torch.equal(got_qkv, want_full[layer][0]), (layer, r)
+            assert torch.equal(got_wo, want_full[layer][1]), (layer, r)
     dev.close()
 
 
