@@ -9,7 +9,7 @@
 // communicating.  Requests then move to "reassigned target pages".
 //
 // These kernels are tiny next to the data movement; each runs as one CTA
-// (plus a wide fill for page tables), with ballot-free block scans.
+// (plus a wide fill for page tables), built on grouped block scans and counts.
 #include <climits>
 
 #include "umm_scan.cuh"

@@ -1,0 +1,113 @@
+"""bench.py on the CPU: the reference arm's JSON line (the oracle, timed), the
+silence of ranks other than 0, and the algorithmic byte model that every GB/s
+figure divides by, checked against the elements the oracle actually writes."""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import bench
+import oracle
+import synth
+from helpers import dims_of, initial_kv_state, kvslot, wslot
+from synth.workloads import TINY, Workload
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+def _run_bench(*args, env_extra=None, timeout=300):
+    env = dict(os.environ)
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, env=env, capture_output=True, text=True,
+                          timeout=timeout)
+
+
+def test_reference_arm_prints_one_complete_line():
+    r = _run_bench("--impl", "reference", "--workload", TINY.name, "--steps", "2", "--warmup", "1")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference"
+    assert j["metric"] == bench.METRIC and j["unit"] == bench.UNIT
+    assert j["value"] > 0 and j["higher_is_better"] is True
+    assert j["steps"] == 2 and j["warmup"] == 1
+    assert j["config"]["workload"] == TINY.name
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == j["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = j["e2e"]
+    assert e2e["value"] == j["value"] and e2e["unit"] == j["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_are_silent():
+    r = _run_bench("--impl", "reference", "--workload", TINY.name, "--steps", "1", "--warmup", "0",
+                   env_extra={"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+# ---------------------------------------------------------------- byte model
+
+def _nonzero_u16(buf: np.ndarray, spans) -> int:
+    u = buf.view(np.uint16)
+    return int(sum(np.count_nonzero(u[a // 2:(a + n) // 2]) for a, n in spans))
+
+
+BYTE_CASES = [
+    TINY,                                                                     # Hkv = P: one copy per head
+    Workload("bytes_rep", P=4, N=1, E=8, H=24, I=16, Hkv=2, D=8, ps=4, R=9, len_a=0, len_b=23, slack=3.0),
+    Workload("bytes_wide", P=2, N=1, E=4, H=8, I=6, Hkv=4, D=4, ps=3, R=7, len_a=1, len_b=17, slack=3.0),
+]
+
+
+@pytest.mark.parametrize("w", BYTE_CASES, ids=lambda w: w.name)
+def test_algorithmic_bytes_equal_elements_the_oracle_moves(w):
+    """Zero the destination slot, make every source element nonzero, run the
+    oracle, count destination elements that became nonzero: that count (x2
+    bytes) is what bench.py charges as written, and the live source elements
+    as read."""
+    d = dims_of(w)
+    L = oracle.layout(d)
+    buf = np.zeros(L["ws_off"], dtype=np.uint8)
+    lens = w.lengths()
+    b = bench.algorithmic_bytes(w, lens)
+    u = buf.view(np.uint16)
+    # ---- weights EP -> TP: EP slot 1 -> TP slot 0
+    for r in range(w.P):
+        a = wslot(L, r, 1) // 2
+        u[a:a + L["wslot_stride"] // 2] = 0x3f80
+    oracle.weights_ep2tp(buf, d)
+    written = _nonzero_u16(buf, [(wslot(L, r, 0), L["wslot_stride"]) for r in range(w.P)])
+    assert 2 * 2 * written == b["weights_per_layer"]        # one read + one write per element moved
+    # ---- KV EP -> TP: EP slot 1 -> TP slot 0 (replicas counted as written)
+    st = initial_kv_state(w, d, L, seed=3)
+    buf[:] = 0
+    for r in range(w.P):
+        a = kvslot(L, r, 1, 0) // 2
+        u[a:a + L["kvslot_stride"] // 2] = 0x3f80
+    assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    tp_spans = [(kvslot(L, r, 0, 0), L["kvslot_stride"]) for r in range(w.P)]
+    wr = 2 * _nonzero_u16(buf, tp_spans)
+    rd = 2 * int(st.lens.sum()) * w.Hkv * w.D * 2            # live K and V rows of the EP pages
+    assert rd + wr == b["kv_ep2tp_per_layer"]
+    # ---- KV TP -> EP: TP slot 0 -> EP slot 1, each head read once (lowest replica)
+    owner2, _, _ = oracle.place(w.P, st.lens, key=st.tp_pos)
+    maxp = w.max_pages_per_req()
+    _, ep_pt2 = oracle.assign_pages(w.P, st.lens, w.ps, maxp,
+                                    synth.permutation(5, 4, L["pages_ep"], w.P), region=owner2, key=st.tp_pos)
+    for r in range(w.P):
+        a = kvslot(L, r, 1, 0) // 2
+        u[a:a + L["kvslot_stride"] // 2] = 0
+    assert oracle.kv_tp2ep(buf, d, st.lens, owner2, ep_pt2, st.tp_pt) == 0
+    wr2 = 2 * _nonzero_u16(buf, [(kvslot(L, r, 1, 0), L["kvslot_stride"]) for r in range(w.P)])
+    assert 2 * wr2 == b["kv_tp2ep_per_layer"]               # read once, written once
+    assert b["tokens"] == int(lens.sum())
