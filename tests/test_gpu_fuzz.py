@@ -19,9 +19,9 @@ from synth.workloads import Workload
 pytestmark = pytest.mark.gpu
 
 
-def random_case(seed: int):
+def random_case(seed: int, ranks=(1, 2, 3, 4, 6, 8, 16)):
     rng = np.random.default_rng(1000 + seed)
-    P = int(rng.choice([1, 2, 3, 4, 6, 8, 16]))
+    P = int(rng.choice(ranks))
     N = int(rng.integers(1, 4))
     E = P * int(rng.integers(1, 4))
     I = P * int(rng.integers(1, 7))
@@ -33,11 +33,11 @@ def random_case(seed: int):
         Hkv = int(rng.choice(divs))                      # Hkv <= P, a divisor
     D = int(rng.integers(1, 20))
     ps = int(rng.integers(1, 33))
-    R = int(rng.integers(0, 40))
+    R = int(rng.integers(0, 40 if P <= 16 else 12))
     Hq = P * int(rng.integers(1, 4)) if rng.random() < 0.6 else 0
+    len_b = int(rng.integers(1, (5 if P <= 16 else 2) * ps + 2))
     return rng, Workload(f"fuzz{seed}", P=P, N=N, E=E, H=H, I=I, Hkv=Hkv, D=D, ps=ps, R=max(R, 1),
-                         len_kind="uniform", len_a=0, len_b=int(rng.integers(1, 5 * ps + 2)), slack=1.0 + P,
-                         Hq=Hq), R
+                         len_kind="uniform", len_a=0, len_b=len_b, slack=1.0 + P, Hq=Hq), R
 
 
 def pool_pages(w: Workload, R: int) -> int:
@@ -70,7 +70,17 @@ def kv_state(rng, w: Workload, d, L: dict, R: int):
 
 @pytest.mark.parametrize("seed", range(24))
 def test_fuzz_parity(seed):
-    rng, w, R = random_case(seed)
+    _fuzz(*random_case(seed), seed)
+
+
+@pytest.mark.parametrize("seed", range(100, 106))
+def test_fuzz_parity_wide_rank_counts(seed):
+    """24 to 64 ranks: group scans and counts over up to 64 groups, one region
+    per rank."""
+    _fuzz(*random_case(seed, ranks=(24, 32, 48, 64)), seed)
+
+
+def _fuzz(rng, w, R, seed):
     ptp = pool_pages(w, R)
     dev = DevUMM(w, seed=seed, pages_tp=ptp, max_requests=R, max_pages=ptp)
     L, d = dev.L, dev.d
