@@ -1,11 +1,14 @@
 // C ABI of libumm: handle, layout of the unified buffer, argument checks,
-// modes, status and per-kernel timing.  Kernels live in umm_weights.cu,
-// umm_kv.cu and umm_requests.cu.
+// modes, status and per-kernel timing.  Kernels live in umm_weights.cu
+// (expert weights), umm_kv_prep.cu and umm_kv.cu (KV descriptor pass and
+// copies), umm_kv_staged.cu (staged KV path), umm_attn.cu (attention weights)
+// and umm_requests.cu (request order, placement, page hand-out).
 //
 // Layout (unified memory manager of "Moebius: Serving Mixture-of-Expert Models
 // with Seamless Runtime Parallelism Switch" (paper review), §4.2, Fig. 7): one
-// region per rank = N+1 weight slots then N+1 KV slots; TP layer l in slot l,
-// EP layer l in slot l+1; a workspace after the P regions.
+// region per rank = N+1 weight slots, N+1 KV slots, then N+1 attention slots;
+// TP layer l in slot l, EP layer l in slot l+1; a workspace after the P
+// regions.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
@@ -91,7 +94,7 @@ int check_dims(const umm_dims* d) {
   return UMM_OK;
 }
 
-// R-1 layout: region = [weight slot 0..N][KV slot 0..N]; W2 at 256 B inside a
+// Layout: region = [weight slot 0..N][KV slot 0..N][attention slot 0..N]; W2 at 256 B inside a
 // weight slot, V at 256 B after K inside a KV slot, slot strides rounded to
 // 4 KiB, region stride to 2 MiB; workspace after the last region.
 void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
@@ -111,7 +114,7 @@ void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
   L->kv_v_off = align_up(half, 256);
   L->kvslot_stride = hkv > 0 ? align_up(L->kv_v_off + half, 4096) : 0;
   L->kvslots_off = (N + 1) * L->wslot_stride;
-  // attention slots (R-16), sized for the full EP copy
+  // attention slots (memory-saving variant), sized for the full EP copy
   const uint64_t hq = (uint64_t)d->attn_q_heads;
   const uint64_t qkv = hq > 0 ? (hq + 2ull * (uint64_t)hkv) * d->head_dim * (uint64_t)d->H * 2ull : 0;
   L->attn_wo_off = align_up(qkv, 256);

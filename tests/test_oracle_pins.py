@@ -155,7 +155,8 @@ def test_weights_exactly_once_tagged():
     got = np.concatenate([np.concatenate([w13_tp(buf, L, d, q, 1).ravel(), w2_tp(buf, L, d, q, 1).ravel()])
                           for q in range(d.P)])
     assert np.array_equal(np.sort(got), np.arange(n13 + d.E * d.H * d.I))
-    # cross-region share: (P-1)/P of the moved elements change rank (§3, R-9)
+    # cross-region share: (P-1)/P of the moved elements change rank (§3); the
+    # rank's own share moves too, from slot l+1 to slot l
     moved_from = []
     for q in range(d.P):
         t13 = w13_tp(buf, L, d, q, 1).astype(np.int64)
@@ -172,7 +173,8 @@ def test_weights_round_trip_identity_and_untouched_bytes():
     buf = fill_regions(L, w, seed=7)
     orig = buf.copy()
     oracle.weights_ep2tp(buf, d)
-    # slot N still holds EP layer N-1 (nothing writes it, R-8)
+    # slot N still holds EP layer N-1: nothing writes it, and bytes that are
+    # not a destination keep their contents
     for r in range(d.P):
         a = wslot(L, r, d.N)
         assert np.array_equal(buf[a:a + L["wslot_stride"]], orig[a:a + L["wslot_stride"]])
@@ -406,7 +408,8 @@ def test_kv_single_request_matches_torch_index_select():
 
 
 def test_kv_untouched_bytes_and_byte_accounting():
-    """R-8: only live token rows are written.  Bytes written per layer EP->TP =
+    """Only live token rows are written; every other byte keeps its contents.
+    Bytes written per layer EP->TP =
     tokens * max(P, Hkv) * D * 2 halves * 2 B; TP->EP = tokens * Hkv * D * 4 B."""
     w = SMALL_KV.with_(kv_sigma=None)
     d, L, st, src = _kv_setup(w)
