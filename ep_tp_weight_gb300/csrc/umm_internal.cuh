@@ -63,6 +63,12 @@ __device__ __forceinline__ void raise_flag(DevStatus* st, unsigned int flag, uns
   atomicCAS(&st->fail_call, 0u, call);
 }
 
+// Pages of a request of `len` tokens (len >= 0), without int32 overflow for
+// lengths near 2^31.
+__device__ __forceinline__ int pages_of(int32_t len, int32_t ps) {
+  return (int)(((long long)len + ps - 1) / ps);
+}
+
 // Everything a kernel needs to address the unified buffer.
 struct Geo {
   uint8_t* base;

@@ -39,15 +39,30 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
   __syncthreads();
   const long long max_len = (long long)maxp * g.ps;
   unsigned long long my_tokens = 0;
-  for (int k = tid; k < R; k += blockDim.x) {
-    const int len = lens[k], o = owner[k];
-    if (len < 0 || (long long)len > max_len || o < 0 || o >= P) {
-      bad = 1;
-      continue;
+  // pages and requests per region: the lanes of a __match_any_sync set (same
+  // region) sum their pages with two 16-bit-half reductions (exact: 32 lanes
+  // x 2^16 < 2^32) and the set's lowest lane adds them with one shared atomic
+  const int lane = tid & 31;
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int k = base + tid;
+    int len = 0, o = -1;
+    if (k < R) {
+      len = lens[k];
+      o = owner[k];
     }
-    atomicAdd(&region_pages[o], (unsigned long long)((len + g.ps - 1) / g.ps));
-    atomicAdd(&region_reqs[o], 1u);
-    my_tokens += (unsigned long long)len;
+    const bool valid = k < R && len >= 0 && (long long)len <= max_len && o >= 0 && o < P;
+    if (k < R && !valid) bad = 1;
+    const unsigned int np = valid ? (unsigned int)pages_of(len, g.ps) : 0u;
+    const unsigned int same = __match_any_sync(0xffffffffu, valid ? o : -1);
+    const unsigned int lo = __reduce_add_sync(same, np & 0xffffu);
+    const unsigned int hi = __reduce_add_sync(same, np >> 16);
+    if (valid) {
+      if (lane == __ffs(same) - 1) {
+        atomicAdd(&region_pages[o], ((unsigned long long)hi << 16) + lo);
+        atomicAdd(&region_reqs[o], (unsigned int)__popc(same));
+      }
+      my_tokens += (unsigned long long)len;
+    }
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) my_tokens += __shfl_xor_sync(0xffffffffu, my_tokens, d);
@@ -88,7 +103,7 @@ kv_prep_scan(Geo g, Ws w, int dir, int32_t R, int32_t maxp, const int32_t* __res
     long long np = 0;
     int grp = 0;
     if (k < R) {
-      np = (lens[k] + g.ps - 1) / g.ps;
+      np = pages_of(lens[k], g.ps);
       grp = owner[k];
     }
     const long long start = group_exclusive_scan(np, grp, P, carry, warp_tot);

@@ -44,7 +44,7 @@ kv_stage_prep(Geo g, Ws w, int32_t R, const int32_t* __restrict__ lens, const in
     if (j < R) {
       const int k = order_req[j];
       len = lens[k];
-      np = (len + g.ps - 1) / g.ps;
+      np = pages_of(len, g.ps);
       grp = owner[k];
     }
     const long long tok = group_exclusive_scan(len, grp, P, carry_t, warp_tot);

@@ -33,10 +33,16 @@ order_kernel(Geo g, Ws w, int32_t R, const int32_t* __restrict__ owner, int32_t*
   if (tid < kMaxGroups) cnt[tid] = 0;
   if (tid == 0) bad = 0;
   __syncthreads();
-  for (int k = tid; k < R; k += blockDim.x) {
-    const int o = owner[k];
-    if (o < 0 || o >= P) bad = 1;
-    else atomicAdd(&cnt[o], 1ull);
+  // requests per rank: one shared atomic per rank and warp (the lanes of a
+  // __match_any_sync set add their count through the set's lowest lane)
+  const int lane = tid & 31;
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int k = base + tid;
+    const int o = k < R ? owner[k] : -1;
+    const bool valid = o >= 0 && o < P;
+    if (k < R && !valid) bad = 1;
+    const unsigned int same = __match_any_sync(0xffffffffu, valid ? o : -1);
+    if (valid && lane == __ffs(same) - 1) atomicAdd(&cnt[o], (unsigned long long)__popc(same));
   }
   __syncthreads();
   if (bad) {
@@ -437,7 +443,7 @@ assign_scan(Geo g, Ws w, int32_t npools, int32_t R, int32_t maxp, const int32_t*
     if (pos < R) {
       k = key ? inv[pos] : pos;
       grp = pool ? pool[k] : 0;
-      np = (lens[k] + g.ps - 1) / g.ps;
+      np = pages_of(lens[k], g.ps);
     }
     const long long pre = group_exclusive_scan(np, grp, npools, carry, warp_tot);
     if (pos < R) start[k] = pre;
@@ -455,7 +461,7 @@ assign_emit(Geo g, Ws w, int32_t R, int32_t maxp, const int32_t* __restrict__ le
   const int warps_total = (gridDim.x * blockDim.x) >> 5;
   const int64_t* start = reinterpret_cast<const int64_t*>(g.base + w.req_off);
   for (int k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < R; k += warps_total) {
-    const int np = (lens[k] + g.ps - 1) / g.ps;
+    const int np = pages_of(lens[k], g.ps);
     const int64_t src = (pool ? (int64_t)pool[k] : 0) * free_stride + start[k];
     int32_t* row = pt + (int64_t)k * maxp;
     for (int p = lane; p < maxp; p += 32) row[p] = p < np ? free_pages[src + p] : -1;
