@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
       if (ok[u]) {
         const uint8_t* src = ep2tp ? p.base + (uint64_t)q * p.region_stride + p.ep_slot + full_off[u]
                                    : shard + shard_off;
-        val[u] = __ldcs(reinterpret_cast<const V*>(src));
+        val[u] = ld_stream(reinterpret_cast<const V*>(src));
         if (ep2tp) full_off[u] = shard_off;   // from here on: where to store
       }
     }
@@ -84,22 +84,22 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
       if (ep2tp) {
-        __stcs(reinterpret_cast<V*>(shard + full_off[u]), val[u]);
+        st_stream(reinterpret_cast<V*>(shard + full_off[u]), val[u]);
       } else {
         for (uint32_t r = 0; r < p.P; ++r)
-          __stcs(reinterpret_cast<V*>(p.base + (uint64_t)r * p.region_stride + p.ep_slot + full_off[u]), val[u]);
+          st_stream(reinterpret_cast<V*>(p.base + (uint64_t)r * p.region_stride + p.ep_slot + full_off[u]), val[u]);
       }
     }
   }
 }
 
 cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
-  constexpr int T = 256, U = 4;
+  constexpr int T = 256, U = 4;   // 16 KiB tiles with 16-byte vectors
   const uint64_t Dh = (uint64_t)g.D, H = (uint64_t)g.H;
   const uint32_t hq = (uint32_t)(g.Hq / g.P), h_tp = (uint32_t)g.h_tp;
   const uint64_t head_bytes = Dh * H * 2, shard_row = (uint64_t)hq * Dh * 2;
   int VB = 2;
-  for (int cand : {16, 8, 4}) {
+  for (int cand : {32, 16, 8, 4}) {
     if (head_bytes % cand == 0 && shard_row % cand == 0) {
       VB = cand;
       break;
@@ -121,7 +121,7 @@ cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   p.h_tp = h_tp;
   p.qkv_vec = (uint32_t)((uint64_t)(hq + 2 * h_tp) * head_bytes / VB);
   p.vr = p.qkv_vec + (uint32_t)(H * shard_row / VB);
-  const uint32_t tile = (uint32_t)(T * U);
+  const uint32_t tile = (uint32_t)(T * (VB == 32 ? U / 2 : U));
   const uint32_t tpr = (p.vr + tile - 1) / tile;
   p.tiles_total = tpr * p.P;
   p.headv = FastDiv((uint32_t)(head_bytes / VB));
@@ -129,6 +129,7 @@ cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   p.tiles_per_rank = FastDiv(tpr);
   if (p.tiles_total == 0) return cudaSuccess;
   switch (VB) {
+    case 32: attn_kernel<32, U / 2, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
     case 16: attn_kernel<16, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
     case 8: attn_kernel<8, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
     case 4: attn_kernel<4, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;

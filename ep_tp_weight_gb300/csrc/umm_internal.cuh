@@ -48,6 +48,39 @@ template <> struct VecT<8> { using T = uint2; };
 template <> struct VecT<4> { using T = uint32_t; };
 template <> struct VecT<2> { using T = unsigned short; };
 
+// 32-byte vectors: 256-bit global loads and stores (sm_100 and later).
+struct alignas(32) u256 {
+  uint32_t w[8];
+};
+template <> struct VecT<32> { using T = u256; };
+
+// Streaming (evict-first) loads and stores of data read or written once.
+template <typename V>
+__device__ __forceinline__ V ld_stream(const V* p) {
+  return __ldcs(p);
+}
+template <>
+__device__ __forceinline__ u256 ld_stream<u256>(const u256* p) {
+  u256 v;
+  asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                 "=r"(v.w[6]), "=r"(v.w[7])
+               : "l"(p));
+  return v;
+}
+template <typename V>
+__device__ __forceinline__ void st_stream(V* p, const V& v) {
+  __stcs(p, v);
+}
+template <>
+__device__ __forceinline__ void st_stream<u256>(u256* p, const u256& v) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :
+               : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]),
+                 "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
+}
+
 // Device view of the workspace status block.
 struct DevStatus {
   unsigned int flags;

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
         p.tok.divmod(rem, tok[u], rem2);
         p.dv.divmod(rem2, h[u], dvv[u]);
         if (v < nvec && tok[u] < (uint32_t)d.ntok)
-          val[u] = __ldcs(reinterpret_cast<const V*>(src_region + c[u] * p.kv_v_off + src_page +
+          val[u] = ld_stream(reinterpret_cast<const V*>(src_region + c[u] * p.kv_v_off + src_page +
                                                       (uint64_t)rem * VB));
         else
           tok[u] = 0xffffffffu;
@@ -88,11 +88,11 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
         if (p.Hkv < p.P) {
           for (uint32_t j = 0; j < p.rep; ++j) {
             const uint32_t q = h[u] * p.rep + j;
-            __stcs(reinterpret_cast<V*>(p.base + (uint64_t)q * p.region_stride + row_off), val[u]);
+            st_stream(reinterpret_cast<V*>(p.base + (uint64_t)q * p.region_stride + row_off), val[u]);
           }
         } else {
           const uint32_t q = h[u] / p.h_tp, hl = h[u] - q * p.h_tp;
-          __stcs(reinterpret_cast<V*>(p.base + (uint64_t)q * p.region_stride + row_off +
+          st_stream(reinterpret_cast<V*>(p.base + (uint64_t)q * p.region_stride + row_off +
                                       (uint64_t)hl * p.head_bytes),
                  val[u]);
         }
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
             q = h / p.h_tp;
             hl = h - q * p.h_tp;
           }
-          val[u] = __ldcs(reinterpret_cast<const V*>(
+          val[u] = ld_stream(reinterpret_cast<const V*>(
               p.base + (uint64_t)q * p.region_stride + p.tp_slot + c[u] * p.kv_v_off + src_page +
               (uint64_t)tok * p.tp_row + (uint64_t)hl * p.head_bytes + (uint64_t)dvv * VB));
         }
@@ -145,18 +145,26 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u])
-          __stcs(reinterpret_cast<V*>(dst_region + c[u] * p.kv_v_off + dst_page + (uint64_t)rem_[u] * VB),
+          st_stream(reinterpret_cast<V*>(dst_region + c[u] * p.kv_v_off + dst_page + (uint64_t)rem_[u] * VB),
                  val[u]);
     }
   }
 }
 
 namespace {
-// EP->TP: 128 threads x 8 vectors (half a 32 KiB K+V page per round);
-// TP->EP: 256 x 4.  Both picked by measurement on GB300 (within ~1% of the
-// neighbouring shapes; 16-vector-per-thread or persistent shapes were slower).
-constexpr int kT_ep2tp = 128, kU_ep2tp = 8;
-constexpr int kT_tp2ep = 256, kU_tp2ep = 4;
+// Threads and vectors per thread of the copies; one round of a CTA loads
+// 16 KiB in every shape below.  Picked by
+// measurement on GB300, full-switch workload, ms per layer EP->TP / TP->EP:
+//   16-byte vectors, 128 x 8 / 256 x 4 (the best 16-byte shapes): 6.211 / 4.131
+//   32-byte vectors: EP->TP 64 x 8: 6.170, 32 x 8: 6.190, 64 x 4: 6.189,
+//   128 x 4: 6.195, 256 x 2: 6.196, 96 x 8: 6.211, 128 x 8: 6.211;
+//   TP->EP 256 x 2: 4.015, 128 x 4: 4.027, 256 x 4: 4.053, 512 x 1: 4.226.
+// 32-byte vectors are used whenever the head size allows them.
+template <int VB>
+struct Shape {
+  static constexpr int T_ep2tp = VB == 32 ? 64 : 128, U_ep2tp = 8;
+  static constexpr int T_tp2ep = 256, U_tp2ep = VB == 32 ? 2 : 4;
+};
 
 // One CTA per descriptor (grid >= live pages): the block scheduler hands a
 // finished CTA's slot to the next page at once, which keeps more loads in
@@ -167,8 +175,9 @@ template <int VB>
 cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t s) {
   if (max_desc <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)(max_desc < 0x7fffffffll ? max_desc : 0x7fffffffll);
-  if (dir == 0) kv_copy_ep2tp<VB, kU_ep2tp, kT_ep2tp><<<grid, kT_ep2tp, 0, s>>>(p);
-  else kv_copy_tp2ep<VB, kU_tp2ep, kT_tp2ep><<<grid, kT_tp2ep, 0, s>>>(p);
+  using S = Shape<VB>;
+  if (dir == 0) kv_copy_ep2tp<VB, S::U_ep2tp, S::T_ep2tp><<<grid, S::T_ep2tp, 0, s>>>(p);
+  else kv_copy_tp2ep<VB, S::U_tp2ep, S::T_tp2ep><<<grid, S::T_tp2ep, 0, s>>>(p);
   return cudaGetLastError();
 }
 }  // namespace
@@ -176,7 +185,8 @@ cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t 
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
                            unsigned int call, cudaStream_t s) {
   int VB = 2;
-  if (g.D % 8 == 0) VB = 16;
+  if (g.D % 16 == 0) VB = 32;
+  else if (g.D % 8 == 0) VB = 16;
   else if (g.D % 4 == 0) VB = 8;
   else if (g.D % 2 == 0) VB = 4;
   const uint32_t per = (uint32_t)VB / 2;
@@ -206,6 +216,7 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.tok = FastDiv((uint32_t)g.Hkv * Dv);
   p.dv = FastDiv(Dv);
   switch (VB) {
+    case 32: return run_copy<32>(p, dir, max_desc, s);
     case 16: return run_copy<16>(p, dir, max_desc, s);
     case 8: return run_copy<8>(p, dir, max_desc, s);
     case 4: return run_copy<4>(p, dir, max_desc, s);

@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) kv_stage_gather(const SParams p, int dir)
               ((uint64_t)d.src_page * p.ps + tok) * p.tp_row + (uint64_t)cv * VB;
       }
       V* dst = reinterpret_cast<V*>(p.send + (((uint64_t)slot * T + t0 + tok) * p.tp_row) + (uint64_t)cv * VB);
-      __stcs(dst, __ldcs(reinterpret_cast<const V*>(src)));
+      st_stream(dst, ld_stream(reinterpret_cast<const V*>(src)));
     }
   }
 }
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) kv_stage_exchange(const SParams p, int di
   const long long T = p.rank_info[3 * p.rank + 2];
   const uint64_t n = 2ull * (dir == 0 ? p.P : p.groups) * (uint64_t)T * p.tp_row / VB;
   for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += (uint64_t)gridDim.x * blockDim.x)
-    __stcs(reinterpret_cast<V*>(p.recv) + v, __ldcs(reinterpret_cast<const V*>(p.send) + v));
+    st_stream(reinterpret_cast<V*>(p.recv) + v, ld_stream(reinterpret_cast<const V*>(p.send) + v));
 }
 
 // stage 3, scatter: recv -> target pages (EP->TP: every TP rank's page;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) kv_stage_scatter(const SParams p, int dir
         dst = p.base + (uint64_t)p.rank * p.region_stride + p.ep_slot + c * p.kv_v_off +
               ((uint64_t)d.dst_page * p.ps + tok) * p.ep_row + (uint64_t)qg * p.h_tp * p.head_bytes +
               (uint64_t)cv * VB;
-      __stcs(reinterpret_cast<V*>(dst), __ldcs(src));
+      st_stream(reinterpret_cast<V*>(dst), ld_stream(src));
     }
   }
 }
