@@ -405,6 +405,7 @@ ATTN_CASES = [
     Workload("attn_p4_hq8_hkv8_odd", P=4, N=2, H=36, Hkv=8, D=6, Hq=8),           # 8-byte vectors
     Workload("attn_p8_hq64_hkv4_d128", P=8, N=2, H=512, Hkv=4, D=128, Hq=64, w_sigma=0.02),
     Workload("attn_p4_h7", P=4, N=2, H=7, Hkv=4, D=3, Hq=4),                       # 2-byte vectors
+    Workload("attn_p4_hq4_d8", P=4, N=2, H=24, Hkv=2, D=8, Hq=4),                   # 16-byte vectors
 ]
 
 
