@@ -503,12 +503,16 @@ class CpuSample:
     KV_REQUESTS = 2048
     KV_ROUNDS = 3
 
-    def __init__(self, w, threads: int):
+    def __init__(self, w, threads: int, kv_requests: int | None = None, kv_rounds: int | None = None,
+                 weight_layers: int | None = None):
         import oracle
         self.oracle = oracle
         self.w = w
         oracle.set_threads(threads)
         self.threads = threads
+        self.KV_REQUESTS = kv_requests or self.KV_REQUESTS
+        self.KV_ROUNDS = kv_rounds or self.KV_ROUNDS
+        self.weight_layers = min(weight_layers or w.N, w.N)
         self.wbuf = None
         self.kbuf = None
         self.abuf = None
@@ -519,7 +523,7 @@ class CpuSample:
             b = algorithmic_bytes(aw, [])
             self.abytes = w.N * (b["attn_ep2tp_per_layer"] + b["attn_tp2ep_per_layer"])
         if w.E:
-            ws = w.with_(Hkv=0, R=0)
+            ws = w.with_(Hkv=0, R=0, N=self.weight_layers)
             self.wd = oracle.Dims(**ws.dims())
             L = oracle.layout(self.wd)
             self.wbuf = np.ones(L["ws_off"], dtype=np.uint8)
@@ -548,7 +552,7 @@ class CpuSample:
         if self.abuf is not None:
             parts.append(f"attention weights of all {self.w.N} layers EP->TP->EP")
         if self.wbuf is not None:
-            parts.append(f"expert weights of all {self.w.N} layers EP->TP->EP")
+            parts.append(f"expert weights of {self.weight_layers} of {self.w.N} layers EP->TP->EP")
         if self.kbuf is not None:
             parts.append(f"KV of {min(self.KV_REQUESTS, self.w.R)} of {self.w.R} requests for 1 layer "
                          f"EP->TP->EP, {self.KV_ROUNDS} times")
@@ -590,11 +594,17 @@ class CpuSample:
 
 
 def cpu_baseline(w):
+    """The oracle on all host cores, plus a smaller sample on one core."""
     threads = os.cpu_count() or 1
     cs = CpuSample(w, threads)
     moved, secs = cs.run()
+    one = CpuSample(w, 1, kv_requests=256, kv_rounds=1, weight_layers=1)
+    m1, s1 = one.run()
+    cs.oracle.set_threads(threads)
     return {"value": round(moved / secs / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": cs.describe() + f"; {moved / 1e9:.1f} GB algorithmic in {secs:.2f} s"}
+            "sample": cs.describe() + f"; {moved / 1e9:.1f} GB algorithmic in {secs:.2f} s",
+            "one_core": {"value": round(m1 / s1 / 1e9, 3), "unit": UNIT, "cores": 1,
+                         "sample": one.describe() + f"; {m1 / 1e9:.1f} GB algorithmic in {s1:.2f} s"}}
 
 
 # ----------------------------------------------------------------------------- main
