@@ -8,11 +8,14 @@ module fails loudly when libumm.so has not been built.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libumm.so")
+# the same ABI, built with every copy-kernel access checked (tests)
+CHECKED_LIB_PATH = os.path.join(_HERE, "libumm_checked.so")
 
 UMM_OK = 0
 UMM_ERR_INVALID_ARG = 1
@@ -24,6 +27,7 @@ UMM_ERR_CUDA = 6
 UMM_ERR_TIMEOUT = 7
 UMM_ERR_DUP_PAGE = 8
 UMM_ERR_BAD_REQUEST = 9
+UMM_ERR_ACCESS = 10
 
 UMM_MODE_EP = 0
 UMM_MODE_TP = 1
@@ -32,6 +36,7 @@ FLAG_BAD_REQUEST = 1
 FLAG_CAPACITY = 2
 FLAG_PAGE_OOB = 4
 FLAG_DUP_PAGE = 8
+FLAG_ACCESS = 16
 
 (K_WEIGHTS_EP2TP, K_WEIGHTS_TP2EP, K_KV_PREP, K_KV_EP2TP, K_KV_TP2EP, K_PLACE, K_ORDER, K_ASSIGN,
  K_ATTN_EP2TP, K_ATTN_TP2EP) = range(10)
@@ -77,7 +82,6 @@ class UmmError(RuntimeError):
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libumm.so is not built ({LIB_PATH}); run ep_tp_weight_gb300.build.build()")
 
-_lib = ctypes.CDLL(LIB_PATH)
 _vp, _i32, _i64, _u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
 _P = ctypes.POINTER
 
@@ -120,12 +124,35 @@ _SIG = {
     "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
     "umm_policy_state": [_vp, _P(_i32), _P(_i64), _P(_i64)],
 }
-for _name, _args in _SIG.items():
-    _f = getattr(_lib, _name)
-    _f.argtypes = _args
-    _f.restype = ctypes.c_int
-_lib.umm_strerror.argtypes = [ctypes.c_int]
-_lib.umm_strerror.restype = ctypes.c_char_p
+
+
+def _bind(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    for name, args in _SIG.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.umm_strerror.argtypes = [ctypes.c_int]
+    lib.umm_strerror.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _bind(LIB_PATH)
+
+
+@contextlib.contextmanager
+def checked_library():
+    """Route every call of this module through libumm_checked.so inside the
+    block (handles made inside must also be destroyed inside)."""
+    global _lib
+    if not os.path.exists(CHECKED_LIB_PATH):
+        raise ImportError(f"libumm_checked.so is not built ({CHECKED_LIB_PATH})")
+    saved = _lib
+    _lib = _bind(CHECKED_LIB_PATH)
+    try:
+        yield
+    finally:
+        _lib = saved
 
 EXPORTED = tuple(_SIG) + ("umm_strerror",)
 

@@ -13,6 +13,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build", "umm")
 LIB = os.path.join(PKG, "libumm.so")
+# the checked build: same sources with UMM_CHECKED (every copy-kernel access
+# tested against its buffer's bounds and alignment), for tests
+CHECKED_OBJDIR = os.path.join(ROOT, "_build", "umm_checked")
+CHECKED_LIB = os.path.join(PKG, "libumm_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -26,21 +30,24 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and not stale():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
-    extra = extra or []
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          checked: bool = False) -> str:
+    """Compile libumm.so (or, with checked=True, libumm_checked.so) in-tree."""
+    lib, objdir = (CHECKED_LIB, CHECKED_OBJDIR) if checked else (LIB, OBJDIR)
+    if not force and not stale(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
+    extra = list(extra or []) + (["-DUMM_CHECKED"] if checked else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = ["nvcc", *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd))
@@ -49,11 +56,18 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.check_call(["nvcc", *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> None:
+    """Both libraries, compiled side by side."""
+    with ThreadPoolExecutor(max_workers=2) as ex:
+        list(ex.map(lambda c: build(force=force, checked=c), (False, True)))
 
 
 if __name__ == "__main__":
     build(force=True, verbose=True)
+    build(force=True, verbose=True, checked=True)

@@ -379,6 +379,7 @@ int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) 
   g.attnslot_stride = u->L.attnslot_stride;
   g.attn_wo_off = u->L.attn_wo_off;
   g.attnslots_off = u->L.attnslots_off;
+  g.flags = reinterpret_cast<unsigned int*>(g.base + u->ws.status);
   g.pages_ep = u->L.pages_ep;
   g.pages_tp = u->L.pages_tp;
   g.h_tp = u->L.h_tp;
@@ -650,7 +651,8 @@ int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags
   if (f & UMM_FLAG_PAGE_OOB) code = UMM_ERR_PAGE_OOB;
   if (f & UMM_FLAG_CAPACITY) code = UMM_ERR_CAPACITY;
   if (f & UMM_FLAG_BAD_REQUEST) code = UMM_ERR_BAD_REQUEST;
-  if (f) {
+  if (f & UMM_FLAG_ACCESS) code = UMM_ERR_ACCESS;   // checked build: a library fault
+  if (f & ~UMM_FLAG_ACCESS) {
     // the first KV reshard at or after the failing call did not run, nor did
     // any later one: the cache is still in the layout that call started from
     for (const KvCall& c : u->kv_log)
@@ -658,6 +660,8 @@ int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags
         u->kv_mode = c.mode_before;
         break;
       }
+  }
+  if (f) {
     uint32_t zero[2] = {0, 0};
     if (cudaMemcpyAsync(u->geo.base + u->ws.status, zero, sizeof(zero), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
@@ -681,6 +685,7 @@ const char* umm_strerror(int code) {
     case UMM_ERR_TIMEOUT: return "bounded device wait timed out";
     case UMM_ERR_DUP_PAGE: return "destination page used twice";
     case UMM_ERR_BAD_REQUEST: return "bad request metadata (length, owner or list position)";
+    case UMM_ERR_ACCESS: return "checked build: an out-of-range or misaligned access was skipped";
     default: return "unknown status";
   }
 }

@@ -25,6 +25,7 @@ struct AParams {
   uint32_t qkv_vec, vr;                       // shard Wqkv vectors, all shard vectors (per rank)
   uint32_t tiles_total;
   FastDiv headv, rowv, tiles_per_rank;
+  Span span;                                  // the P regions
 };
 
 // the full-layout head held at local head slot b of TP rank q (-1: a key or
@@ -76,7 +77,8 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
       if (ok[u]) {
         const uint8_t* src = ep2tp ? p.base + (uint64_t)q * p.region_stride + p.ep_slot + full_off[u]
                                    : shard + shard_off;
-        val[u] = ld_stream(reinterpret_cast<const V*>(src));
+        ok[u] = access_ok<VB>(p.span, src);
+        if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(src));
         if (ep2tp) full_off[u] = shard_off;   // from here on: where to store
       }
     }
@@ -84,10 +86,12 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
       if (ep2tp) {
-        st_stream(reinterpret_cast<V*>(shard + full_off[u]), val[u]);
+        if (access_ok<VB>(p.span, shard + full_off[u])) st_stream(reinterpret_cast<V*>(shard + full_off[u]), val[u]);
       } else {
-        for (uint32_t r = 0; r < p.P; ++r)
-          st_stream(reinterpret_cast<V*>(p.base + (uint64_t)r * p.region_stride + p.ep_slot + full_off[u]), val[u]);
+        for (uint32_t r = 0; r < p.P; ++r) {
+          uint8_t* const dst = p.base + (uint64_t)r * p.region_stride + p.ep_slot + full_off[u];
+          if (access_ok<VB>(p.span, dst)) st_stream(reinterpret_cast<V*>(dst), val[u]);
+        }
       }
     }
   }
@@ -127,6 +131,7 @@ cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   p.headv = FastDiv((uint32_t)(head_bytes / VB));
   p.rowv = FastDiv((uint32_t)(shard_row / VB));
   p.tiles_per_rank = FastDiv(tpr);
+  p.span = g.regions();
   if (p.tiles_total == 0) return cudaSuccess;
   switch (VB) {
     case 32: attn_kernel<32, U / 2, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;

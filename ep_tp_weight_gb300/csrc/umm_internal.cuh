@@ -102,6 +102,31 @@ __device__ __forceinline__ int pages_of(int32_t len, int32_t ps) {
   return (int)(((long long)len + ps - 1) / ps);
 }
 
+// The buffer a kernel's vector accesses must lie in.  In the checked build
+// (UMM_CHECKED) every access is tested against it and against the vector's
+// alignment; a failing access is skipped and raises UMM_FLAG_ACCESS.  In the
+// normal build the test compiles away.
+struct Span {
+  const uint8_t* lo;
+  const uint8_t* hi;
+  unsigned int* flags;
+};
+
+template <int VB>
+__device__ __forceinline__ bool access_ok(const Span& s, const void* a) {
+#ifdef UMM_CHECKED
+  const uint8_t* b = static_cast<const uint8_t*>(a);
+  if (b < s.lo || b + VB > s.hi || (reinterpret_cast<uintptr_t>(b) & (uintptr_t)(VB - 1))) {
+    atomicOr(s.flags, UMM_FLAG_ACCESS);
+    return false;
+  }
+#else
+  (void)s;
+  (void)a;
+#endif
+  return true;
+}
+
 // Everything a kernel needs to address the unified buffer.
 struct Geo {
   uint8_t* base;
@@ -110,6 +135,12 @@ struct Geo {
   int32_t P, E, H, I, N, Hkv, D, ps, w13_split, Hq;
   int64_t pages_ep, pages_tp, h_tp;
   uint64_t attnslot_stride, attn_wo_off, attnslots_off;
+  unsigned int* flags;     // the workspace status block's flags word
+
+  // the P regions: every fused copy stays inside them
+  __host__ __device__ Span regions() const {
+    return Span{base, base + (uint64_t)P * region_stride, flags};
+  }
 };
 
 // Workspace carve-up (byte offsets from the buffer base).

@@ -32,6 +32,7 @@ struct KVParams {
   uint32_t half_vec;           // vectors in one half (K or V) of an EP page
   long long pages_tp;
   FastDiv half, tok, dv;       // divisors: half_vec, Hkv*Dv, Dv
+  Span span;                   // the P regions
 };
 
 // The descriptor a CTA works on for grid position di: in TP-page order
@@ -74,11 +75,13 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
         p.half.divmod(v, c[u], rem);
         p.tok.divmod(rem, tok[u], rem2);
         p.dv.divmod(rem2, h[u], dvv[u]);
-        if (v < nvec && tok[u] < (uint32_t)d.ntok)
-          val[u] = ld_stream(reinterpret_cast<const V*>(src_region + c[u] * p.kv_v_off + src_page +
-                                                      (uint64_t)rem * VB));
-        else
+        if (v < nvec && tok[u] < (uint32_t)d.ntok) {
+          const uint8_t* const src = src_region + c[u] * p.kv_v_off + src_page + (uint64_t)rem * VB;
+          if (access_ok<VB>(p.span, src)) val[u] = ld_stream(reinterpret_cast<const V*>(src));
+          else tok[u] = 0xffffffffu;
+        } else {
           tok[u] = 0xffffffffu;
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -88,13 +91,13 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
         if (p.Hkv < p.P) {
           for (uint32_t j = 0; j < p.rep; ++j) {
             const uint32_t q = h[u] * p.rep + j;
-            st_stream(reinterpret_cast<V*>(p.base + (uint64_t)q * p.region_stride + row_off), val[u]);
+            uint8_t* const dst = p.base + (uint64_t)q * p.region_stride + row_off;
+            if (access_ok<VB>(p.span, dst)) st_stream(reinterpret_cast<V*>(dst), val[u]);
           }
         } else {
           const uint32_t q = h[u] / p.h_tp, hl = h[u] - q * p.h_tp;
-          st_stream(reinterpret_cast<V*>(p.base + (uint64_t)q * p.region_stride + row_off +
-                                      (uint64_t)hl * p.head_bytes),
-                 val[u]);
+          uint8_t* const dst = p.base + (uint64_t)q * p.region_stride + row_off + (uint64_t)hl * p.head_bytes;
+          if (access_ok<VB>(p.span, dst)) st_stream(reinterpret_cast<V*>(dst), val[u]);
         }
       }
     }
@@ -137,9 +140,12 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
             q = h / p.h_tp;
             hl = h - q * p.h_tp;
           }
-          val[u] = ld_stream(reinterpret_cast<const V*>(
-              p.base + (uint64_t)q * p.region_stride + p.tp_slot + c[u] * p.kv_v_off + src_page +
-              (uint64_t)tok * p.tp_row + (uint64_t)hl * p.head_bytes + (uint64_t)dvv * VB));
+          const uint8_t* const src = p.base + (uint64_t)q * p.region_stride + p.tp_slot + c[u] * p.kv_v_off +
+                                     src_page + (uint64_t)tok * p.tp_row + (uint64_t)hl * p.head_bytes +
+                                     (uint64_t)dvv * VB;
+          ok[u] = access_ok<VB>(p.span, src) &&
+                  access_ok<VB>(p.span, dst_region + c[u] * p.kv_v_off + dst_page + (uint64_t)rem * VB);
+          if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(src));
         }
       }
 #pragma unroll
@@ -215,6 +221,7 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.half = FastDiv(p.half_vec);
   p.tok = FastDiv((uint32_t)g.Hkv * Dv);
   p.dv = FastDiv(Dv);
+  p.span = g.regions();
   switch (VB) {
     case 32: return run_copy<32>(p, dir, max_desc, s);
     case 16: return run_copy<16>(p, dir, max_desc, s);

@@ -79,6 +79,7 @@ struct SParams {
   int32_t R, rank;
   uint64_t region_stride, kv_v_off, ep_slot, tp_slot, ep_row, tp_row, head_bytes;
   uint32_t ps, Hkv, P, h_tp, rep, groups;   // groups = Hkv / h_tp head groups
+  Span regions, staging;                    // the P regions; the caller's staging buffer
 };
 
 // token offset of descriptor di inside its rank's stream
@@ -122,8 +123,9 @@ __global__ void __launch_bounds__(256) kv_stage_gather(const SParams p, int dir)
         src = p.base + (uint64_t)q * p.region_stride + p.tp_slot + c * p.kv_v_off +
               ((uint64_t)d.src_page * p.ps + tok) * p.tp_row + (uint64_t)cv * VB;
       }
-      V* dst = reinterpret_cast<V*>(p.send + (((uint64_t)slot * T + t0 + tok) * p.tp_row) + (uint64_t)cv * VB);
-      st_stream(dst, ld_stream(reinterpret_cast<const V*>(src)));
+      uint8_t* const dst = p.send + (((uint64_t)slot * T + t0 + tok) * p.tp_row) + (uint64_t)cv * VB;
+      if (access_ok<VB>(p.regions, src) && access_ok<VB>(p.staging, dst))
+        st_stream(reinterpret_cast<V*>(dst), ld_stream(reinterpret_cast<const V*>(src)));
     }
   }
 }
@@ -136,7 +138,9 @@ __global__ void __launch_bounds__(256) kv_stage_exchange(const SParams p, int di
   const long long T = p.rank_info[3 * p.rank + 2];
   const uint64_t n = 2ull * (dir == 0 ? p.P : p.groups) * (uint64_t)T * p.tp_row / VB;
   for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += (uint64_t)gridDim.x * blockDim.x)
-    st_stream(reinterpret_cast<V*>(p.recv) + v, ld_stream(reinterpret_cast<const V*>(p.send) + v));
+    if (access_ok<VB>(p.staging, reinterpret_cast<V*>(p.send) + v) &&
+        access_ok<VB>(p.staging, reinterpret_cast<V*>(p.recv) + v))
+      st_stream(reinterpret_cast<V*>(p.recv) + v, ld_stream(reinterpret_cast<const V*>(p.send) + v));
 }
 
 // stage 3, scatter: recv -> target pages (EP->TP: every TP rank's page;
@@ -168,7 +172,8 @@ __global__ void __launch_bounds__(256) kv_stage_scatter(const SParams p, int dir
         dst = p.base + (uint64_t)p.rank * p.region_stride + p.ep_slot + c * p.kv_v_off +
               ((uint64_t)d.dst_page * p.ps + tok) * p.ep_row + (uint64_t)qg * p.h_tp * p.head_bytes +
               (uint64_t)cv * VB;
-      st_stream(reinterpret_cast<V*>(dst), ld_stream(src));
+      if (access_ok<VB>(p.staging, src) && access_ok<VB>(p.regions, dst))
+        st_stream(reinterpret_cast<V*>(dst), ld_stream(src));
     }
   }
 }
@@ -199,6 +204,8 @@ cudaError_t launch_kv_staged(const Geo& g, const Ws& w, int dir, int32_t R, cons
   const uint64_t half = kv_stage_bytes(g) / 2;
   p.send = stage;
   p.recv = stage + half;
+  p.regions = g.regions();
+  p.staging = Span{stage, stage + 2 * half, g.flags};
   p.desc = reinterpret_cast<const umm_kv_desc*>(g.base + w.desc);
   p.st = reinterpret_cast<const DevStatus*>(g.base + w.status);
   p.order_req = reinterpret_cast<const int32_t*>(g.base + w.req_inv);

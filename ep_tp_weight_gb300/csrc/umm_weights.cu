@@ -34,6 +34,7 @@ struct WParams {
   uint32_t tiles_total;
   FastDiv hv, two_i, i_d, ip_d, two_ip, iv, ipv, tiles_per_region;
   int split;
+  Span ep_span, tp_span;              // where EP-side and TP-side addresses must lie
 };
 
 template <int VB, int U, int T>
@@ -91,20 +92,24 @@ __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) 
                      trow * p.w2_tp_row_bytes + (uint64_t)cc * VB;
       }
     }
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      ok[u] = ep_addr[u] && access_ok<VB>(p.ep_span, ep_addr[u]) && access_ok<VB>(p.tp_span, tp_addr[u]);
     if (ep2tp) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ep_addr[u]) val[u] = ld_stream(reinterpret_cast<const V*>(ep_addr[u]));
+        if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(ep_addr[u]));
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ep_addr[u]) st_stream(reinterpret_cast<V*>(tp_addr[u]), val[u]);
+        if (ok[u]) st_stream(reinterpret_cast<V*>(tp_addr[u]), val[u]);
     } else {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ep_addr[u]) val[u] = ld_stream(reinterpret_cast<const V*>(tp_addr[u]));
+        if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(tp_addr[u]));
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ep_addr[u]) st_stream(reinterpret_cast<V*>(ep_addr[u]), val[u]);
+        if (ok[u]) st_stream(reinterpret_cast<V*>(ep_addr[u]), val[u]);
     }
   }
 }
@@ -173,6 +178,8 @@ WParams layer_params(const Geo& g, int layer, int VB) {
   p.ipv = FastDiv(Ip / per);
   p.tiles_per_region = FastDiv(tpr);
   p.split = g.w13_split;
+  p.ep_span = g.regions();
+  p.tp_span = g.regions();
   return p;
 }
 
@@ -198,6 +205,7 @@ struct XParams {
   uint32_t tiles_total;
   FastDiv tiles_pair;                 // tiles13 + tiles2
   FastDiv pd;                         // P
+  Span stage_span, region_span;
 };
 
 template <int VB, int U, int T>
@@ -214,15 +222,17 @@ __global__ void __launch_bounds__(T) exchange_kernel(const XParams p, int to_tp)
     uint8_t* tp = p.base + (uint64_t)q * p.region_stride +
                   (w13 ? p.tp_w13_off + (uint64_t)r * p.seg13 : p.tp_w2_off + (uint64_t)r * p.seg2);
     V val[U];
+    bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint64_t o = off0 + (uint64_t)(u * T + threadIdx.x) * VB;
-      if (o < seg) val[u] = ld_stream(reinterpret_cast<const V*>((to_tp ? st : tp) + o));
+      ok[u] = o < seg && access_ok<VB>(p.stage_span, st + o) && access_ok<VB>(p.region_span, tp + o);
+      if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>((to_tp ? st : tp) + o));
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint64_t o = off0 + (uint64_t)(u * T + threadIdx.x) * VB;
-      if (o < seg) st_stream(reinterpret_cast<V*>(const_cast<uint8_t*>(to_tp ? tp : st) + o), val[u]);
+      if (ok[u]) st_stream(reinterpret_cast<V*>(const_cast<uint8_t*>(to_tp ? tp : st) + o), val[u]);
     }
   }
 }
@@ -245,6 +255,8 @@ cudaError_t run_exchange(const Geo& g, int layer, int VB, const uint8_t* stage, 
   x.tiles_total = (x.tiles13 + x.tiles2) * x.P * x.P;
   x.tiles_pair = FastDiv(x.tiles13 + x.tiles2);
   x.pd = FastDiv(x.P);
+  x.stage_span = Span{stage, stage + weights_stage_bytes(g), g.flags};
+  x.region_span = g.regions();
   if (x.tiles_total == 0) return cudaSuccess;
   switch (VB) {
     case 16: exchange_kernel<16, kU, kT><<<x.tiles_total, kT, 0, s>>>(x, to_tp); break;
@@ -279,6 +291,7 @@ cudaError_t launch_weights_staged(const Geo& g, int ep2tp, int layer, uint8_t* s
   p.tp_w13_off = 0;
   p.tp_w2_off = El * 2 * Ip * H * 2;
   p.tp_eoff_per_r = 0;
+  p.tp_span = Span{stage, stage + weights_stage_bytes(g), g.flags};
   cudaError_t e;
   if (ep2tp) {   // permute into per-peer blocks, then exchange into the TP slots
     if ((e = run_any(p, VB, 1, s)) != cudaSuccess) return e;

@@ -47,6 +47,13 @@
  *  - The library never aborts, traps or throws across this ABI.
  *  - A handle is not thread-safe: issue its calls from one host thread, with
  *    the buffer's device current.
+ *  - Checked build.  libumm_checked.so is the same library compiled with
+ *    UMM_CHECKED: before every vector load or store, the copy kernels (weights,
+ *    KV, attention, and the staged variants) test the address against the
+ *    buffer it must lie in (the P regions, or the caller's staging buffer) and
+ *    against the vector's alignment.  A failing access is skipped and raises
+ *    UMM_FLAG_ACCESS (status UMM_ERR_ACCESS).  The checked build serves tests;
+ *    the flag can only come from a library fault, never from caller input.
  */
 #ifndef UMM_H_
 #define UMM_H_
@@ -69,6 +76,8 @@ extern "C" {
 #define UMM_ERR_DUP_PAGE     8  /* two live pages would be written to one destination page */
 #define UMM_ERR_BAD_REQUEST  9  /* length < 0 or > max_pages_per_req*page_size, owner or
                                    list position out of range                             */
+#define UMM_ERR_ACCESS      10  /* checked build only: a kernel formed an address outside
+                                   its buffer or off its vector alignment (skipped)       */
 
 #define UMM_MODE_EP 0
 #define UMM_MODE_TP 1
@@ -140,6 +149,7 @@ typedef struct {
 #define UMM_FLAG_CAPACITY    2u
 #define UMM_FLAG_PAGE_OOB    4u
 #define UMM_FLAG_DUP_PAGE    8u
+#define UMM_FLAG_ACCESS     16u   /* checked build only, see UMM_ERR_ACCESS */
 
 /* One page-indexed work descriptor (§4.3): the live tokens of logical page
  * `page` of request `req`.  Descriptors are grouped by the rank whose bytes

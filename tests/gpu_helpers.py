@@ -12,6 +12,11 @@ from synth.workloads import Workload
 
 _tables: dict[float, torch.Tensor] = {}
 
+# Guard bands before and after every test buffer, filled with patterns that
+# close() checks: a kernel that writes outside the unified buffer fails the test.
+GUARD = 64 << 10
+GUARD_LO, GUARD_HI = 0xA5, 0x5A
+
 
 def table_dev(sigma: float) -> torch.Tensor:
     if sigma not in _tables:
@@ -46,7 +51,10 @@ class DevUMM:
         self.d = dims_of(w, **{k: v for k, v in over.items() if k not in ("weight_mode", "kv_mode")})
         self.dims = lib_dims(w, **over)
         self.nbytes = umm.umm_required_bytes(self.dims)
-        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device="cuda")
+        self.raw = torch.empty(self.nbytes + 2 * GUARD, dtype=torch.uint8, device="cuda")
+        self.raw[:GUARD].fill_(GUARD_LO)
+        self.raw[GUARD + self.nbytes:].fill_(GUARD_HI)
+        self.buf = self.raw[GUARD:GUARD + self.nbytes]
         self.h = umm.umm_create(self.dims, self.buf, self.nbytes)
         self.L = umm.umm_layout(self.h)
         if fill:
@@ -63,12 +71,20 @@ class DevUMM:
     def status(self):
         return umm.umm_status_sync(self.h)
 
+    def guards_intact(self) -> bool:
+        torch.cuda.synchronize()
+        return bool((self.raw[:GUARD] == GUARD_LO).all().item() and
+                    (self.raw[GUARD + self.nbytes:] == GUARD_HI).all().item())
+
     def close(self) -> None:
         if self.h:
             umm.umm_destroy(self.h)
             self.h = None
+        intact = self.raw is None or self.guards_intact()
         self.buf = None
+        self.raw = None
         torch.cuda.empty_cache()
+        assert intact, "a kernel wrote into the guard bands around the unified buffer"
 
 
 def i32(a) -> torch.Tensor:

@@ -43,15 +43,27 @@ def test_library_exports_every_declared_entry_point(umm):
     assert set(names) == set(umm.EXPORTED)
 
 
-def test_library_exports_nothing_undeclared(umm):
+@pytest.mark.parametrize("which", ["LIB_PATH", "CHECKED_LIB_PATH"])
+def test_library_exports_nothing_undeclared(umm, which):
+    """Both builds (normal and checked) export exactly the declared C ABI."""
     import shutil
     import subprocess
     if not shutil.which("nm"):
         pytest.skip("nm not available")
-    out = subprocess.run(["nm", "-D", "--defined-only", umm.LIB_PATH], capture_output=True, text=True).stdout
+    out = subprocess.run(["nm", "-D", "--defined-only", getattr(umm, which)], capture_output=True,
+                         text=True).stdout
     c_symbols = {ln.split()[-1] for ln in out.splitlines()
                  if " T " in ln and not ln.split()[-1].startswith(("_Z", "cuda", "__", "_"))}
     assert c_symbols == set(declared_functions())
+
+
+def test_checked_library_loads_with_the_same_signatures(umm):
+    with umm.checked_library():
+        assert umm._lib._name == umm.CHECKED_LIB_PATH
+        for n in umm.EXPORTED:
+            assert hasattr(umm._lib, n), n
+        assert umm.strerror(umm.UMM_ERR_ACCESS).startswith("checked build")
+    assert umm._lib._name == umm.LIB_PATH
 
 
 def test_binding_constants_match_header(umm):
