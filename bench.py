@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-staged", action="store_true")
+    ap.add_argument("--phase-sweep", action="store_true",
+                    help="instead of the benchmark line: the full-switch shape at several request counts, "
+                         "one JSON line each with ms per phase (weights, request metadata, descriptor pass, KV)")
     return ap.parse_args()
 
 
@@ -227,7 +230,7 @@ def whole_job_gbs(bytes_per_step: int, steps: int, ms_total_max: float, world: i
 
 # ----------------------------------------------------------------------------- the GPU run
 
-def run_umm(args, rank, world, local_rank):
+def run_umm(args, rank, world, local_rank, w=None):
     import torch
     import ep_tp_weight_gb300 as umm
     dist = None
@@ -235,7 +238,7 @@ def run_umm(args, rank, world, local_rank):
         import torch.distributed as dist
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = ALL[args.workload]
+    w = w or ALL[args.workload]
     lens_h = w.lengths()
     R = len(lens_h)
     maxp = w.max_pages_per_req() if R else 1
@@ -609,6 +612,37 @@ def cpu_baseline(w):
 
 # ----------------------------------------------------------------------------- main
 
+def phase_sweep(args):
+    """The full-switch shape (weights + KV) at growing request counts, as the
+    page's switch-cost breakdown by phase: the weights are a fixed floor, the
+    KV grows with occupancy, the request metadata stays nearly flat."""
+    args.no_graph = args.no_staged = args.no_e2e = True
+    for R in (16, 128, 512, 1024, 2048):
+        w = FULL_SWITCH.with_(name=f"{FULL_SWITCH.name}_{R}req", R=R)
+        # a TP pool large enough that each rank's EP pool (pages_tp * h_tp / Hkv)
+        # holds its share under the greedy rule: at most the mean plus the
+        # longest request, plus one partial page per request
+        pages = synth.npages(w.lengths(), w.ps)
+        used, m = int(pages.sum()), w.Hkv // w.h_tp
+        bound = used / w.P + int(pages.max()) + R / w.P + 1
+        w = w.with_(slack=max(FULL_SWITCH.slack, 1.02 * m * bound / used))
+        r = run_umm(args, 0, 1, 0, w=w)
+        prof, n = r["prof"], args.steps
+
+        def ms(*kinds):
+            return round(sum(prof[k][1] for k in kinds) / n, 3)
+
+        line = {"phase_sweep": True, "workload": w.name, "requests": R, "tokens": int(r["lens"].sum()),
+                "ms_per_round_trip": round(r["ms_total"] / n, 3),
+                "ms_per_switch": {"ep2tp": round(r["ms_ep2tp"], 3), "tp2ep": round(r["ms_tp2ep"], 3)},
+                "phases_ms_per_round_trip": {"weights": ms("weights_ep2tp", "weights_tp2ep"),
+                                             "request_metadata": ms("order", "place", "assign"),
+                                             "descriptor_pass": ms("kv_prep"),
+                                             "kv": ms("kv_ep2tp", "kv_tp2ep")},
+                "clocks": r["clocks"]}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -640,6 +674,11 @@ def main():
                                  "sample": "each step: " + cs.describe()},
                 "e2e": {"value": round(val, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
+        return
+
+    if args.phase_sweep:
+        if rank == 0:
+            phase_sweep(args)
         return
 
     if world > 1:
