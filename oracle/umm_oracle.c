@@ -23,9 +23,10 @@
  *   §4.3, Table 1: one read and one write per moved element.
  *
  * Readings of points the page leaves open (each is restated where it is used):
- *   R-1 buffer layout: region r = [weight slot 0..N][KV slot 0..N]; KV uses the
- *       same N+1 slot mapping as the weights; the P regions are followed by a
- *       workspace.  Alignments: W2 at 256 B inside a slot, slot strides at
+ *   R-1 buffer layout: region r = [weight slot 0..N][KV slot 0..N][attention
+ *       slot 0..N] (attention slots only when there are attention weights,
+ *       R-16); KV and attention use the same N+1 slot mapping as the weights;
+ *       the P regions are followed by a workspace.  Alignments: W2 at 256 B inside a slot, slot strides at
  *       4 KiB, region stride at 2 MiB.  K half then V half in a KV slot, each
  *       half sized for the TP view.
  *   R-2 TP rank q's 2I/P rows of W13 = gate rows [q*Ip,(q+1)*Ip) followed by
