@@ -484,6 +484,57 @@ def test_switch_entry_points_equal_oracle(w):
     dev.close()
 
 
+def test_many_round_trips_stay_exact():
+    """40 EP->TP->EP round trips through umm_switch_* on one handle, each with
+    fresh free lists, the KV pool two-thirds full so that the copies walk it
+    through the call-tagged TP-page schedule (stale entries of earlier calls
+    must be ignored), and the status read only at the end: equal to the
+    oracle step for step."""
+    w = Workload("many_trips", P=4, N=2, E=8, H=32, I=16, Hkv=2, D=16, ps=4, R=24, len_a=1, len_b=30,
+                 slack=1.5, Hq=8)
+    lens = w.lengths().copy()
+    trips = 40
+    maxp = int((lens.max() + w.ps - 1) // w.ps)
+    used = int(((lens + w.ps - 1) // w.ps).sum())
+    m = w.Hkv // w.h_tp
+    ptp = (int(1.5 * used) + m - 1) // m * m
+    dev = DevUMM(w, seed=29, pages_tp=ptp, max_requests=len(lens), max_pages=ptp)
+    d, L = dev.d, dev.L
+    R, P = len(lens), d.P
+    owner, _, _ = oracle.place(P, lens)
+    _, ep_pt = oracle.assign_pages(P, lens, d.ps, maxp, synth.permutation(1, 2, L["pages_ep"], rows=P), region=owner)
+    ref = dev.host()
+    d_owner, d_ep_pt = i32(owner), i32(ep_pt)
+    d_pos = torch.empty(R, dtype=torch.int32, device="cuda")
+    d_tp_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
+    d_local = torch.empty(R, dtype=torch.int32, device="cuda")
+    for trip in range(trips):
+        tp_free = synth.permutation(100 + trip, 3, L["pages_tp"], rows=1)
+        ep_free = synth.permutation(100 + trip, 4, L["pages_ep"], rows=P)
+        d_lens = i32(lens)
+        umm.umm_switch_ep2tp(dev.h, R, maxp, d_lens, d_owner, d_ep_pt, i32(tp_free), L["pages_tp"], d_pos, d_tp_pt)
+        pos = oracle.request_order(P, owner)
+        _, tp_pt = oracle.assign_pages(1, lens, d.ps, maxp, tp_free, key=pos)
+        oracle.weights_ep2tp(ref, d)
+        oracle.attn_ep2tp(ref, d)
+        assert oracle.kv_ep2tp(ref, d, lens, owner, ep_pt, tp_pt) == 0
+        n_owner = torch.empty(R, dtype=torch.int32, device="cuda")
+        n_ep_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
+        umm.umm_switch_tp2ep(dev.h, R, maxp, d_lens, d_pos, d_tp_pt, i32(ep_free), L["pages_ep"], L["pages_ep"],
+                             n_owner, d_local, n_ep_pt)
+        owner, _, _ = oracle.place(P, lens, key=pos)
+        _, ep_pt = oracle.assign_pages(P, lens, d.ps, maxp, ep_free, region=owner, key=pos)
+        oracle.weights_tp2ep(ref, d)
+        oracle.attn_tp2ep(ref, d)
+        assert oracle.kv_tp2ep(ref, d, lens, owner, ep_pt, tp_pt) == 0
+        d_owner, d_ep_pt = n_owner, n_ep_pt
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(d_owner.cpu().numpy(), owner)
+    np.testing.assert_array_equal(d_ep_pt.cpu().numpy(), ep_pt)
+    np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
+
+
 def test_request_metadata_errors_are_refused_on_device():
     """Bad owners, pools, list positions and pool shortage raise flags and
     leave the outputs untouched."""
