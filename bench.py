@@ -63,7 +63,10 @@ def parse():
     ap.add_argument("--phase-sweep", action="store_true",
                     help="instead of the benchmark line: the full-switch shape at several request counts, "
                          "one JSON line each with ms per phase (weights, request metadata, descriptor pass, KV)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be at least 1 and --warmup at least 0")
+    return args
 
 
 # ----------------------------------------------------------------------------- bytes model
