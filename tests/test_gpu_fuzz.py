@@ -121,3 +121,80 @@ def _fuzz(rng, w, R, seed):
     assert dev.status() == (0, 0)
     np.testing.assert_array_equal(dev.host(), ref)
     dev.close()
+
+
+def _code_of(flags: int) -> int:
+    """The status a set of flags reports (highest first: bad request, capacity,
+    page out of range, duplicate page), as include/umm.h documents."""
+    for bit, code in ((oracle.F_BAD_REQUEST, umm.UMM_ERR_BAD_REQUEST), (oracle.F_CAPACITY, umm.UMM_ERR_CAPACITY),
+                      (oracle.F_PAGE_OOB, umm.UMM_ERR_PAGE_OOB), (oracle.F_DUP_PAGE, umm.UMM_ERR_DUP_PAGE)):
+        if flags & bit:
+            return code
+    return umm.UMM_OK
+
+
+def _live(lens, ps):
+    return [(k, p) for k in range(len(lens)) for p in range((int(lens[k]) + ps - 1) // ps)]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_fuzz_invalid_metadata_is_refused(seed):
+    """One to three random corruptions of a valid KV call (bad lengths or
+    owners, page ids out of range, a destination or TP source page used twice):
+    the device raises exactly the oracle's validation flags, writes nothing, and
+    the handle works again after the status read."""
+    rng = np.random.default_rng(5000 + seed)
+    P = int(rng.choice([2, 3, 4, 8]))
+    Hkv = int(rng.choice([h for h in (1, 2, 4, 8, 16) if h % P == 0 or P % h == 0]))
+    w = Workload(f"bad{seed}", P=P, N=2, Hkv=Hkv, D=int(rng.choice([4, 8, 16])), ps=int(rng.integers(2, 9)),
+                 R=int(rng.integers(4, 20)), len_kind="uniform", len_a=1, len_b=40, slack=1.0 + P)
+    R = w.R
+    ptp = pool_pages(w, R)
+    dev = DevUMM(w, seed=seed, pages_tp=ptp, max_requests=R, max_pages=ptp)
+    d, L = dev.d, dev.L
+    ok, lens, maxp, owner, ep_pt, tp_pt, owner2, ep_pt2 = kv_state(rng, w, d, L, R)
+    assert ok
+    direction = int(rng.integers(2))
+    a = {"lens": lens.copy(), "owner": (owner if direction == 0 else owner2).copy(),
+         "ep_pt": (ep_pt if direction == 0 else ep_pt2).copy(), "tp_pt": tp_pt.copy()}
+    live = _live(lens, w.ps)
+    kinds = ["neg_len", "long_len", "bad_owner", "ep_oob", "tp_oob", "dup_dst"] + (["dup_tp"] if direction else [])
+    for kind in rng.choice(kinds, size=int(rng.integers(1, 4))):
+        k = int(rng.integers(R))
+        if kind == "neg_len":
+            a["lens"][k] = -int(rng.integers(1, 5))
+        elif kind == "long_len":
+            a["lens"][k] = maxp * w.ps + int(rng.integers(1, 5))
+        elif kind == "bad_owner":
+            a["owner"][k] = int(rng.choice([-1, P, P + 3]))
+        elif kind in ("ep_oob", "tp_oob") and live:
+            kk, p = live[int(rng.integers(len(live)))]
+            pool = L["pages_ep"] if kind == "ep_oob" else L["pages_tp"]
+            a["ep_pt" if kind == "ep_oob" else "tp_pt"][kk, p] = int(rng.choice([-1, pool, pool + 7]))
+        elif kind in ("dup_dst", "dup_tp") and len(live) > 1:
+            i, j = rng.choice(len(live), size=2, replace=False)
+            (k1, p1), (k2, p2) = live[int(i)], live[int(j)]
+            if kind == "dup_tp" or direction == 0:
+                a["tp_pt"][k2, p2] = a["tp_pt"][k1, p1]
+            elif a["owner"][k1] == a["owner"][k2]:
+                a["ep_pt"][k2, p2] = a["ep_pt"][k1, p1]
+    want = oracle.kv_validate(d, direction, a["lens"], a["owner"], a["ep_pt"], a["tp_pt"])
+    ref = dev.host()
+    if direction == 1:
+        umm.umm_set_modes(dev.h, umm.UMM_MODE_EP, umm.UMM_MODE_TP)
+    fn = umm.reshard_kv_ep2tp if direction == 0 else umm.reshard_kv_tp2ep
+    fn(dev.h, R, maxp, i32(a["lens"]), i32(a["owner"]), i32(a["ep_pt"]), i32(a["tp_pt"]))
+    assert dev.status() == (_code_of(want), want)
+    assert dev.status() == (0, 0)
+    if want:
+        # refused: nothing written, and the KV mode is back to the call's source
+        np.testing.assert_array_equal(dev.host(), ref)
+        assert umm.umm_get_modes(dev.h)[1] == (umm.UMM_MODE_TP if direction else umm.UMM_MODE_EP)
+        # the handle works again: the valid call of the same direction
+        owner_ok = owner if direction == 0 else owner2
+        ep_ok = ep_pt if direction == 0 else ep_pt2
+        fn(dev.h, R, maxp, i32(lens), i32(owner_ok), i32(ep_ok), i32(tp_pt))
+        (oracle.kv_ep2tp if direction == 0 else oracle.kv_tp2ep)(ref, d, lens, owner_ok, ep_ok, tp_pt)
+        assert dev.status() == (0, 0)
+        np.testing.assert_array_equal(dev.host(), ref)
+    dev.close()
