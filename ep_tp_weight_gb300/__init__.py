@@ -143,7 +143,8 @@ _lib = _bind(LIB_PATH)
 @contextlib.contextmanager
 def checked_library():
     """Route every call of this module through libumm_checked.so inside the
-    block (handles made inside must also be destroyed inside)."""
+    block (handles made inside must also be destroyed inside).  It swaps a
+    module global: use it from one thread, as the tests do."""
     global _lib
     if not os.path.exists(CHECKED_LIB_PATH):
         raise ImportError(f"libumm_checked.so is not built ({CHECKED_LIB_PATH})")

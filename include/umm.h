@@ -71,7 +71,8 @@ extern "C" {
 #define UMM_ERR_MODE         3  /* e.g. EP->TP requested while the data is already TP     */
 #define UMM_ERR_CAPACITY     4  /* target pool / descriptor space too small (§4.5)         */
 #define UMM_ERR_PAGE_OOB     5  /* a page id outside its pool                             */
-#define UMM_ERR_CUDA         6  /* a CUDA runtime call failed                             */
+#define UMM_ERR_CUDA         6  /* a CUDA runtime call failed (a launch of a multi-kernel
+                                   call: the kernels enqueued before it stay enqueued)    */
 #define UMM_ERR_TIMEOUT      7  /* reserved: a bounded device wait gave up                */
 #define UMM_ERR_DUP_PAGE     8  /* two live pages would be written to one destination page */
 #define UMM_ERR_BAD_REQUEST  9  /* length < 0 or > max_pages_per_req*page_size, owner or
