@@ -150,3 +150,37 @@ def test_create_rejects_misaligned_and_small_buffers(umm):
     with pytest.raises(umm.UmmError) as ei:
         umm.umm_create(d, 0x100000, 16)
     assert ei.value.code == umm.UMM_ERR_CAPACITY
+
+
+def test_c_program_uses_the_abi(umm, tmp_path):
+    """tests/c_abi_check.c, compiled as C99 with -Wall -Wextra -Werror against
+    include/umm.h and linked with libumm.so, calls the host-side entry points;
+    what it prints equals what the Python binding gets."""
+    import shutil
+    import subprocess
+    from pathlib import Path
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not available")
+    root = Path(__file__).resolve().parent.parent
+    lib_dir = Path(umm.LIB_PATH).parent
+    exe = tmp_path / "c_abi_check"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", str(root / "include"),
+                    str(root / "tests" / "c_abi_check.c"), "-L", str(lib_dir), "-lumm",
+                    f"-Wl,-rpath,{lib_dir}", "-o", str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = dict(ln.split(" ", 1) for ln in out.splitlines())
+    assert int(got["entry_points"]) == len(umm.EXPORTED)
+    assert int(got["sizeof_dims"]) == ctypes.sizeof(umm.UmmDims)
+    assert int(got["sizeof_layout"]) == ctypes.sizeof(umm.UmmLayout)
+    dims = umm.make_dims(P=8, E=128, H=2048, I=768, N=8, Hkv=4, D=128, ps=16, pages_tp=441304,
+                         max_requests=2048, max_pages=441304)
+    assert int(got["required_bytes"]) == umm.umm_required_bytes(dims)
+    L = umm.umm_layout_for_dims(dims)
+    for k in ("region_stride", "wslot_stride", "kvslot_stride", "kvslots_off", "ws_off", "pages_ep", "h_tp"):
+        assert int(got[k]) == L[k], k
+    assert int(got["bad_experts"]) == umm.UMM_ERR_INVALID_ARG
+    assert int(got["bad_heads"]) == umm.UMM_ERR_INVALID_ARG
+    assert int(got["null_handle"]) == umm.UMM_ERR_INVALID_ARG
+    assert got["strerror_capacity"] == umm.strerror(umm.UMM_ERR_CAPACITY)
+    assert (int(got["policy_last_decision"]), int(got["policy_mode"]), int(got["policy_switches"])) == \
+        (umm.POLICY_TO_EP, umm.UMM_MODE_EP, 1)
