@@ -302,6 +302,48 @@ def test_kv_and_full_switch_fullsize(w):
     dev.close()
 
 
+def test_full_switch_soak_100_round_trips():
+    """100 round trips of the full switch through umm_switch_*, on one handle,
+    with new free lists on every trip (pages move each time).  Afterwards
+    every weight slot that holds an EP layer is bit-identical to its start,
+    and sampled KV elements of every layer sit in their requests' final EP
+    pages with their original values."""
+    w = FULL_SWITCH
+    dev = DevUMM(w, seed=w.seed)
+    run = KVRun(dev)
+    h, L, d, P, R, maxp = dev.h, dev.L, dev.d, w.P, run.R, run.maxp
+    d_lens = i32(run.lens)
+    d_owner, d_ep_pt = i32(run.owner0), i32(run.ep_pt0)
+    n_owner, n_ep_pt = torch.empty_like(d_owner), torch.empty_like(d_ep_pt)
+    d_local = torch.empty_like(d_owner)
+    d_pos = torch.empty(R, dtype=torch.int32, device="cuda")
+    d_tp_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
+    for trip in range(100):
+        tp_free = i32(synth.permutation(1000 + trip, 3, L["pages_tp"], rows=1))
+        ep_free = i32(synth.permutation(1000 + trip, 4, L["pages_ep"], rows=P))
+        umm.umm_switch_ep2tp(h, R, maxp, d_lens, d_owner, d_ep_pt, tp_free, L["pages_tp"], d_pos, d_tp_pt)
+        umm.umm_switch_tp2ep(h, R, maxp, d_lens, d_pos, d_tp_pt, ep_free, L["pages_ep"], L["pages_ep"], n_owner,
+                             d_local, n_ep_pt)
+        d_owner, n_owner = n_owner, d_owner
+        d_ep_pt, n_ep_pt = n_ep_pt, d_ep_pt
+    assert dev.status() == (0, 0)
+    _check_weights_round_trip(dev)
+    owner_t, ep_pt_t = d_owner.cpu().numpy(), d_ep_pt.cpu().numpy()
+    rng = np.random.default_rng(9)
+    k, tok, c, hh, e, layer, _ = _kv_samples(run, rng, SAMPLES)
+    q0 = np.where(w.Hkv >= w.P, hh // max(1, w.Hkv // w.P), hh * max(1, w.P // w.Hkv))
+    src = np.empty(SAMPLES, np.int64)
+    dst = np.empty(SAMPLES, np.int64)
+    for i in range(SAMPLES):
+        p, t = divmod(int(tok[i]), w.ps)
+        src[i], _ = oracle.kv_elem(d, int(run.owner0[k[i]]), int(q0[i]), int(run.ep_pt0[k[i], p]), 0, t,
+                                   int(c[i]), int(hh[i]), int(e[i]), int(layer[i]) + 1, 0)
+        dst[i], _ = oracle.kv_elem(d, int(owner_t[k[i]]), int(q0[i]), int(ep_pt_t[k[i], p]), 0, t,
+                                   int(c[i]), int(hh[i]), int(e[i]), int(layer[i]) + 1, 0)
+    np.testing.assert_array_equal(_gather(dev, dst // 2), _expect(dev, src // 2, True))
+    dev.close()
+
+
 def _attn_views(dev: DevUMM, r: int, slot: int, full: bool):
     """(QKV heads, Wo) of one attention slot as device tensors: EP (full) or
     TP (shard) view, the shapes of §3.1's attention part."""
