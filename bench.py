@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-staged", action="store_true")
+    ap.add_argument("--overlap", action="store_true",
+                    help="run the weight reshards of each switch on the handle's side stream "
+                         "(umm_set_switch_overlap); per-kernel times then overlap")
     ap.add_argument("--phase-sweep", action="store_true",
                     help="instead of the benchmark line: the full-switch shape at several request counts, "
                          "one JSON line each with ms per phase (weights, request metadata, descriptor pass, KV)")
@@ -252,6 +255,8 @@ def run_umm(args, rank, world, local_rank, w=None):
     nbytes = umm.umm_required_bytes(dims)
     buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)          # the one allocation (§4.2)
     h = umm.umm_create(dims, buf, nbytes)
+    if getattr(args, "overlap", False):
+        umm.umm_set_switch_overlap(h, True)
     L = umm.umm_layout(h)
     s = torch.cuda.Stream(device=dev)
     # initial contents: every element = synth value of its index
@@ -636,6 +641,7 @@ def phase_sweep(args):
             return round(sum(prof[k][1] for k in kinds) / n, 3)
 
         line = {"phase_sweep": True, "workload": w.name, "requests": R, "tokens": int(r["lens"].sum()),
+                "switch_overlap": bool(args.overlap),
                 "ms_per_round_trip": round(r["ms_total"] / n, 3),
                 "ms_per_switch": {"ep2tp": round(r["ms_ep2tp"], 3), "tp2ep": round(r["ms_tp2ep"], 3)},
                 "phases_ms_per_round_trip": {"weights": ms("weights_ep2tp", "weights_tp2ep"),
@@ -655,6 +661,8 @@ def main():
     config = {"workload": w.name, "P": w.P, "layers": w.N, "experts": w.E, "hidden": w.H, "attn_q_heads": w.Hq,
               "intermediate": w.I, "requests": w.R, "kv_heads": w.Hkv, "head_dim": w.D, "page_size": w.ps,
               "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas{world}"}
+    if args.overlap:
+        config["switch_overlap"] = True
 
     if args.impl == "reference":
         if rank != 0:

@@ -119,6 +119,7 @@ _SIG = {
     "umm_set_attn_mode": [_vp, _i32],
     "umm_switch_ep2tp": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
     "umm_switch_tp2ep": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp],
+    "umm_set_switch_overlap": [_vp, _i32],
     "umm_policy_create": [_vp, _P(_vp)],
     "umm_policy_destroy": [_vp],
     "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
@@ -342,6 +343,10 @@ def umm_switch_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, tp_pos, t
     _ck(_lib.umm_switch_tp2ep(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(tp_pos), _ptr(tp_page_table),
                               _ptr(ep_free_pages), int(ep_free_stride), int(ep_free_count), _ptr(ep_owner),
                               _ptr(local_pos), _ptr(ep_page_table), _stream(stream)), "umm_switch_tp2ep")
+
+
+def umm_set_switch_overlap(h: int, enable: bool = True) -> None:
+    _ck(_lib.umm_set_switch_overlap(h, 1 if enable else 0), "umm_set_switch_overlap")
 
 
 def umm_kv_check_capacity(h: int, target_kv_mode: int, R: int, h_seq_lens, h_ep_owner=None) -> int:

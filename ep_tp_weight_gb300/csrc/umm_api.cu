@@ -51,6 +51,11 @@ struct umm {
   int64_t launches = 0;   // kernels enqueued by this handle
   int64_t prof_n[UMM_K_COUNT] = {};
   double prof_ms[UMM_K_COUNT] = {};
+  // opt-in (umm_set_switch_overlap): the weight reshards of a one-call switch
+  // run on a side stream, beside the request bookkeeping and the KV reshard
+  bool overlap = false;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace {
@@ -399,6 +404,9 @@ int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) 
 
 int umm_destroy(umm_t* u) {
   if (!u) return UMM_ERR_INVALID_ARG;
+  if (u->side) cudaStreamDestroy(u->side);   // resources go once its work is done
+  if (u->ev_fork) cudaEventDestroy(u->ev_fork);
+  if (u->ev_join) cudaEventDestroy(u->ev_join);
   for (auto& p : u->pending) {
     cudaEventDestroy(p.a);
     cudaEventDestroy(p.b);
@@ -557,6 +565,53 @@ int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
                     stream);
 }
 
+int umm_set_switch_overlap(umm_t* u, int32_t enable) {
+  if (!u) return UMM_ERR_INVALID_ARG;
+  if (enable && !u->side) {
+    int dev_now = -1;
+    if (cudaGetDevice(&dev_now) != cudaSuccess || dev_now != u->device) return UMM_ERR_INVALID_ARG;
+    if (cudaStreamCreateWithFlags(&u->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&u->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&u->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+      if (u->side) cudaStreamDestroy(u->side);
+      if (u->ev_fork) cudaEventDestroy(u->ev_fork);
+      u->side = nullptr;
+      u->ev_fork = u->ev_join = nullptr;
+      return UMM_ERR_CUDA;
+    }
+  }
+  u->overlap = enable != 0;
+  return UMM_OK;
+}
+
+namespace {
+
+// With overlap on, and both weights (or attention weights) and live KV to
+// move, the weight reshards go to the side stream: it first waits for
+// `stream` (fork), and `stream` waits for it at the end (join), so the call
+// stays one ordered unit on `stream` (and capturable into one graph).
+struct SwitchStreams {
+  umm* u;
+  cudaStream_t main;
+  bool forked = false;
+  SwitchStreams(umm* uu, void* stream, bool use_side) : u(uu), main(as_stream(stream)) {
+    if (use_side && cudaEventRecord(u->ev_fork, main) == cudaSuccess &&
+        cudaStreamWaitEvent(u->side, u->ev_fork, 0) == cudaSuccess)
+      forked = true;
+  }
+  void* weights() const { return forked ? static_cast<void*>(u->side) : static_cast<void*>(main); }
+  int join() {
+    if (!forked) return UMM_OK;
+    forked = false;
+    if (cudaEventRecord(u->ev_join, u->side) != cudaSuccess || cudaStreamWaitEvent(main, u->ev_join, 0) != cudaSuccess)
+      return UMM_ERR_CUDA;
+    return UMM_OK;
+  }
+  ~SwitchStreams() { join(); }
+};
+
+}  // namespace
+
 int umm_switch_ep2tp(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_lens, const int32_t* d_ep_owner,
                      const int32_t* d_ep_page_table, const int32_t* d_tp_free_pages, int64_t tp_free_count,
                      int32_t* d_tp_pos, int32_t* d_tp_page_table, void* stream) {
@@ -571,9 +626,10 @@ int umm_switch_ep2tp(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_len
     if (rc) return rc;
     if (R > 0 && (!d_tp_free_pages || !d_tp_pos || tp_free_count < 0)) return UMM_ERR_INVALID_ARG;
   }
+  SwitchStreams ss(u, stream, u->overlap && (w || a) && kv && R > 0);
   int rc = UMM_OK;
-  if (w && (rc = reshard_weights(u, 1, stream))) return rc;
-  if (a && (rc = reshard_attn(u, 1, stream))) return rc;
+  if (w && (rc = reshard_weights(u, 1, ss.weights()))) return rc;
+  if (a && (rc = reshard_attn(u, 1, ss.weights()))) return rc;
   if (!kv) return UMM_OK;
   if (R > 0) {
     if ((rc = gather_requests_ep2tp(u, R, d_ep_owner, d_tp_pos, stream))) return rc;
@@ -581,7 +637,8 @@ int umm_switch_ep2tp(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_len
                                tp_free_count, d_tp_page_table, maxp, stream)))
       return rc;
   }
-  return reshard_kv(u, 0, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream);
+  if ((rc = reshard_kv(u, 0, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream))) return rc;
+  return ss.join();
 }
 
 int umm_switch_tp2ep(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_lens, const int32_t* d_tp_pos,
@@ -600,17 +657,24 @@ int umm_switch_tp2ep(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_len
                   (u->dims.P > 1 && ep_free_stride < ep_free_count)))
       return UMM_ERR_INVALID_ARG;
   }
+  SwitchStreams ss(u, stream, u->overlap && (w || a) && kv && R > 0);
   int rc = UMM_OK;
+  auto weights = [&]() {
+    if (w && (rc = reshard_weights(u, 0, ss.weights()))) return rc;
+    if (a && (rc = reshard_attn(u, 0, ss.weights()))) return rc;
+    return UMM_OK;
+  };
+  if (ss.forked && weights()) return rc;            // beside the bookkeeping below
   if (kv && R > 0) {
     if ((rc = place_requests_tp2ep(u, R, d_seq_lens, d_tp_pos, d_ep_owner, d_local_pos, stream))) return rc;
     if ((rc = umm_assign_pages(u, u->dims.P, R, d_seq_lens, d_ep_owner, d_tp_pos, d_ep_free_pages, ep_free_stride,
                                ep_free_count, d_ep_page_table, maxp, stream)))
       return rc;
   }
-  if (w && (rc = reshard_weights(u, 0, stream))) return rc;
-  if (a && (rc = reshard_attn(u, 0, stream))) return rc;
+  if (!ss.forked && weights()) return rc;
   if (!kv) return UMM_OK;
-  return reshard_kv(u, 1, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream);
+  if ((rc = reshard_kv(u, 1, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream))) return rc;
+  return ss.join();
 }
 
 int umm_kv_check_capacity(const umm_t* u, int32_t target_kv_mode, int32_t R, const int32_t* h_seq_lens,

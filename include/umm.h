@@ -344,6 +344,20 @@ int umm_switch_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
                      int64_t ep_free_stride, int64_t ep_free_count, int32_t* d_ep_owner, int32_t* d_local_pos,
                      int32_t* d_ep_page_table, void* stream);
 
+/* Opt-in (default off): in umm_switch_ep2tp / umm_switch_tp2ep the weight
+ * and attention-weight reshards run on a side stream of the handle, beside
+ * the request bookkeeping and the KV reshard on `stream`.  They touch
+ * disjoint slots, so the result is the same; the side stream waits for
+ * `stream` at the start of the call and `stream` waits for it at the end, so
+ * a call stays one ordered unit on `stream` (and one unit in a captured
+ * graph).  It shortens switches with little KV to move, where the fixed
+ * weight copy dominates.  Per-kernel times read through umm_profile_* then
+ * overlap.  The first enable creates the side stream and two events: make it
+ * with the buffer's device current, before any stream capture.  Applies only
+ * when the call has both weights (or attention weights) and live KV.
+ * Errors: INVALID_ARG (null handle, other device current), CUDA. */
+int umm_set_switch_overlap(umm_t* u, int32_t enable);
+
 /* §4.5 capacity check on the host, before committing a switch: UMM_OK if the
  * target layout's KV pools hold the requests (TP: all pages in one pool of
  * pages_tp; EP: each owner's pages within pages_ep), else UMM_ERR_CAPACITY.

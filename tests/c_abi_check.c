@@ -28,7 +28,7 @@ int main(void) {
       (any_fn)reshard_kv_tp2ep_staged, (any_fn)reshard_attn_ep2tp, (any_fn)reshard_attn_tp2ep,
       (any_fn)umm_get_attn_mode, (any_fn)umm_set_attn_mode, (any_fn)umm_switch_ep2tp,
       (any_fn)umm_switch_tp2ep, (any_fn)umm_policy_create, (any_fn)umm_policy_destroy,
-      (any_fn)umm_policy_step, (any_fn)umm_policy_state};
+      (any_fn)umm_policy_step, (any_fn)umm_policy_state, (any_fn)umm_set_switch_overlap};
   for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i)
     if (!fns[i]) return 10;
   printf("entry_points %zu\n", sizeof(fns) / sizeof(fns[0]));

@@ -347,6 +347,42 @@ def test_switch_captured_in_a_cuda_graph():
     dev.close()
 
 
+def test_overlapped_switch_captured_in_a_cuda_graph():
+    """With the side stream on, one call still forms one unit: a captured
+    umm_switch_ep2tp (weights on the side stream, bookkeeping and KV on the
+    capturing stream) replays to the oracle's result, and nothing ran during
+    the capture."""
+    w = Workload("cap_ovl", P=4, N=2, E=8, H=64, I=32, Hkv=2, D=16, ps=4, R=5, len_a=1, len_b=25, slack=3.0)
+    dev = DevUMM(w, seed=8)
+    umm.umm_set_switch_overlap(dev.h, True)
+    d, L = dev.d, dev.L
+    st = initial_kv_state(w, d, L, seed=4)
+    R, maxp = len(st.lens), st.ep_pt.shape[1]
+    tp_free = synth.permutation(6, 3, L["pages_tp"], rows=1)
+    d_pos = torch.empty(R, dtype=torch.int32, device="cuda")
+    d_tp_pt = torch.empty((R, maxp), dtype=torch.int32, device="cuda")
+    args = (i32(st.lens), i32(st.owner), i32(st.ep_pt), i32(tp_free))
+    ref = dev.host()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            umm.umm_switch_ep2tp(dev.h, R, maxp, *args[:3], args[3], L["pages_tp"], d_pos, d_tp_pt, s)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dev.host(), ref)        # capture ran nothing
+    g.replay()
+    torch.cuda.synchronize()
+    pos = oracle.request_order(d.P, st.owner)
+    _, tp_pt = oracle.assign_pages(1, st.lens, d.ps, maxp, tp_free, key=pos)
+    oracle.weights_ep2tp(ref, d)
+    assert oracle.kv_ep2tp(ref, d, st.lens, st.owner, st.ep_pt, tp_pt) == 0
+    np.testing.assert_array_equal(dev.host(), ref)
+    np.testing.assert_array_equal(d_tp_pt.cpu().numpy(), tp_pt)
+    assert dev.status() == (0, 0)
+    dev.close()
+
+
 # ------------------------------------------------------------------ staged (collective-style) comparison path
 
 @pytest.mark.parametrize("w", [TINY, W_CASES[1], W_CASES[3], W_CASES[5]], ids=lambda w: w.name)
@@ -439,11 +475,14 @@ def test_attn_needs_attention_dims():
 @pytest.mark.parametrize("w", [TINY.with_(Hq=4), Workload("switch_mid", P=4, N=3, E=8, H=40, I=24, Hkv=2, D=8, ps=4,
                                                             R=20, len_a=1, len_b=37, slack=3.0, Hq=8)],
                          ids=lambda w: w.name)
-def test_switch_entry_points_equal_oracle(w):
+@pytest.mark.parametrize("overlap", [False, True], ids=["serial", "overlap"])
+def test_switch_entry_points_equal_oracle(w, overlap):
     """umm_switch_ep2tp / umm_switch_tp2ep: weights, attention, request
     order, page hand-out and KV in one call each; the same bytes and metadata
-    as the oracle's step-by-step definition."""
+    as the oracle's step-by-step definition, with the weights on the caller's
+    stream or on the handle's side stream (overlap)."""
     dev = DevUMM(w, seed=17)
+    umm.umm_set_switch_overlap(dev.h, overlap)
     d, L = dev.d, dev.L
     st = initial_kv_state(w, d, L, seed=3)
     R, maxp = len(st.lens), st.ep_pt.shape[1]
