@@ -198,6 +198,11 @@ struct ProfScope {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? UMM_OK : UMM_ERR_CUDA; }
 
+// Layer t of a call's copies runs as a programmatic dependent of layer t-1
+// (launch_chain).  Not while per-kernel timing is on: its events sit between
+// the launches, and each kernel is then timed on its own.
+bool chained(const umm* u, int t) { return t > 0 && !u->prof; }
+
 int check_kv_args(const umm* u, int32_t R, int32_t maxp, const void* a, const void* b, const void* c,
                   const void* d) {
   if (!u || u->dims.num_kv_heads == 0) return UMM_ERR_INVALID_ARG;
@@ -231,7 +236,7 @@ int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, co
   for (int t = 0; t < N; ++t) {
     const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
     ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
-    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s));
+    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(u, t)));
     if (rc) return rc;
     if (max_desc > 0) ++u->launches;
   }
@@ -249,7 +254,7 @@ int reshard_weights(umm* u, int ep2tp, void* stream) {
   for (int t = 0; t < N; ++t) {
     const int layer = ep2tp ? t : N - 1 - t;
     ProfScope ps(u, ep2tp ? UMM_K_WEIGHTS_EP2TP : UMM_K_WEIGHTS_TP2EP, s);
-    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s));
+    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s, chained(u, t)));
     if (rc) return rc;
     ++u->launches;
   }
@@ -448,7 +453,7 @@ static int reshard_attn(umm_t* u, int ep2tp, void* stream) {
   for (int t = 0; t < N; ++t) {
     const int layer = ep2tp ? t : N - 1 - t;
     ProfScope ps(u, ep2tp ? UMM_K_ATTN_EP2TP : UMM_K_ATTN_TP2EP, s);
-    int rc = cuda_rc(uk::launch_attn(u->geo, ep2tp, layer, s));
+    int rc = cuda_rc(uk::launch_attn(u->geo, ep2tp, layer, s, chained(u, t)));
     if (rc) return rc;
     ++u->launches;
   }

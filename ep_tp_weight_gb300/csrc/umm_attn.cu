@@ -10,7 +10,7 @@
 // ranks).  TP->EP is the all-gather: every shard element is read once and
 // stored into all P full copies (key/value heads from their lowest replica).
 // N+1 slots per layer as for the expert weights; layers ascending (EP->TP) or
-// descending (TP->EP), one launch per layer.
+// descending (TP->EP), one launch per layer, chained (griddep_wait).
 #include "umm_internal.cuh"
 
 namespace uk {
@@ -46,6 +46,7 @@ __device__ __forceinline__ int full_head(const AParams& p, uint32_t q, uint32_t 
 template <int VB, int U, int T>
 __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
   using V = typename VecT<VB>::T;
+  griddep_launch_dependents();
   for (uint32_t tile = blockIdx.x; tile < p.tiles_total; tile += gridDim.x) {
     uint32_t q, lt;
     p.tiles_per_rank.divmod(tile, q, lt);
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
         if (ep2tp) full_off[u] = shard_off;   // from here on: where to store
       }
     }
+    griddep_wait();
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
@@ -95,9 +97,10 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
       }
     }
   }
+  griddep_wait();
 }
 
-cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
+cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s, bool chained) {
   constexpr int T = 256, U = 4;   // 16 KiB tiles with 16-byte vectors
   const uint64_t Dh = (uint64_t)g.D, H = (uint64_t)g.H;
   const uint32_t hq = (uint32_t)(g.Hq / g.P), h_tp = (uint32_t)g.h_tp;
@@ -133,14 +136,14 @@ cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
   p.tiles_per_rank = FastDiv(tpr);
   p.span = g.regions();
   if (p.tiles_total == 0) return cudaSuccess;
+  const unsigned grid = p.tiles_total;
   switch (VB) {
-    case 32: attn_kernel<32, U / 2, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
-    case 16: attn_kernel<16, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
-    case 8: attn_kernel<8, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
-    case 4: attn_kernel<4, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
-    default: attn_kernel<2, U, T><<<p.tiles_total, T, 0, s>>>(p, ep2tp); break;
+    case 32: return launch_chain(attn_kernel<32, U / 2, T>, grid, T, s, chained, p, ep2tp);
+    case 16: return launch_chain(attn_kernel<16, U, T>, grid, T, s, chained, p, ep2tp);
+    case 8: return launch_chain(attn_kernel<8, U, T>, grid, T, s, chained, p, ep2tp);
+    case 4: return launch_chain(attn_kernel<4, U, T>, grid, T, s, chained, p, ep2tp);
+    default: return launch_chain(attn_kernel<2, U, T>, grid, T, s, chained, p, ep2tp);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace uk

@@ -81,6 +81,39 @@ __device__ __forceinline__ void st_stream<u256>(u256* p, const u256& v) {
                : "memory");
 }
 
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).  The layer
+// copies of one reshard call run as a chain: layer k+1 is launched with
+// programmatic stream serialization, so its CTAs may start while layer k's
+// last wave drains.  Layer k+1 only reads a slot that no launch of the chain
+// writes (ascending: EP slot k+2; descending: TP slot k-1), so it loads before
+// waiting; it writes the slot layer k reads, so every store comes after
+// griddep_wait(), which returns once the previous grid has completed and its
+// memory is visible (at once when the launch carried no such attribute).
+// Every CTA passes griddep_wait() before it exits, so a chained grid never
+// completes ahead of its predecessor.  A hardware dependency, not a spin.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches kern<<<grid, block, 0, s>>>(args...), as a programmatic dependent
+// of the previous launch on s when `chained`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chain(void (*kern)(KArgs...), unsigned grid, unsigned block, cudaStream_t s, bool chained,
+                         Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device view of the workspace status block.
 struct DevStatus {
   unsigned int flags;
@@ -163,8 +196,10 @@ struct Ws {
 };
 
 // ---- launchers (enqueue only; all arguments already validated) ----
-cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s);
-cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s);
+// chained: launch as a programmatic dependent of the previous layer's copy
+// (griddep_wait above); false for the first layer of a call.
+cudaError_t launch_attn(const Geo& g, int ep2tp, int layer, cudaStream_t s, bool chained);
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, bool chained);
 // The staged comparison path (permute + exchange through `stage`).
 uint64_t weights_stage_bytes(const Geo& g);
 cudaError_t launch_weights_staged(const Geo& g, int ep2tp, int layer, uint8_t* stage, cudaStream_t s,
@@ -178,7 +213,7 @@ cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_
 // the grid walks the TP page pool (descriptors in TP-page order, empty pages
 // exit at once); otherwise it walks the descriptor list.
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
-                           unsigned int call, cudaStream_t s);
+                           unsigned int call, cudaStream_t s, bool chained);
 
 // The staged comparison path for the KV cache (gather -> exchange -> scatter
 // per rank through `stage`; the descriptor pass must have run first).

@@ -9,7 +9,8 @@
 // per element).
 //
 // One launch per layer (kv_copy_*: one CTA per TP page, or per descriptor when
-// the pool is sparsely used), driven by the descriptors of the descriptor pass
+// the pool is sparsely used; layers after the first chained, griddep_wait),
+// driven by the descriptors of the descriptor pass
 // (umm_kv_prep.cu).  Nothing is written to the cache unless that pass raised
 // no flag.
 #include "umm_scan.cuh"
@@ -56,7 +57,11 @@ __device__ __forceinline__ bool fetch_desc(const KVParams& p, unsigned long long
 template <int VB, int U, int T>
 __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
   using V = typename VecT<VB>::T;
-  if (read_flags(p.st)) return;
+  griddep_launch_dependents();
+  if (read_flags(p.st)) {
+    griddep_wait();
+    return;
+  }
   const unsigned long long nd = p.sched ? (unsigned long long)p.pages_tp : p.st->ndesc;
   const uint32_t nvec = 2 * p.half_vec;
   for (unsigned long long di = blockIdx.x; di < nd; di += gridDim.x) {
@@ -83,6 +88,7 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
           tok[u] = 0xffffffffu;
         }
       }
+      griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (tok[u] == 0xffffffffu) continue;
@@ -102,6 +108,7 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
       }
     }
   }
+  griddep_wait();
 }
 
 // TP -> EP: each vector of the destination EP page is read from the lowest TP
@@ -109,7 +116,11 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
 template <int VB, int U, int T>
 __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
   using V = typename VecT<VB>::T;
-  if (read_flags(p.st)) return;
+  griddep_launch_dependents();
+  if (read_flags(p.st)) {
+    griddep_wait();
+    return;
+  }
   const unsigned long long nd = p.sched ? (unsigned long long)p.pages_tp : p.st->ndesc;
   const uint32_t nvec = 2 * p.half_vec;
   for (unsigned long long di = blockIdx.x; di < nd; di += gridDim.x) {
@@ -148,6 +159,7 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
           if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(src));
         }
       }
+      griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u])
@@ -155,6 +167,7 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
                  val[u]);
     }
   }
+  griddep_wait();
 }
 
 namespace {
@@ -178,18 +191,17 @@ struct Shape {
 // (measured on GB300: ~6.72 vs ~6.13 TB/s EP->TP at the full-switch size).
 // The kernels still stride by gridDim.x, so any grid size is correct.
 template <int VB>
-cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t s) {
+cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t s, bool chained) {
   if (max_desc <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)(max_desc < 0x7fffffffll ? max_desc : 0x7fffffffll);
   using S = Shape<VB>;
-  if (dir == 0) kv_copy_ep2tp<VB, S::U_ep2tp, S::T_ep2tp><<<grid, S::T_ep2tp, 0, s>>>(p);
-  else kv_copy_tp2ep<VB, S::U_tp2ep, S::T_tp2ep><<<grid, S::T_tp2ep, 0, s>>>(p);
-  return cudaGetLastError();
+  if (dir == 0) return launch_chain(kv_copy_ep2tp<VB, S::U_ep2tp, S::T_ep2tp>, grid, S::T_ep2tp, s, chained, p);
+  return launch_chain(kv_copy_tp2ep<VB, S::U_tp2ep, S::T_tp2ep>, grid, S::T_tp2ep, s, chained, p);
 }
 }  // namespace
 
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
-                           unsigned int call, cudaStream_t s) {
+                           unsigned int call, cudaStream_t s, bool chained) {
   int VB = 2;
   if (g.D % 16 == 0) VB = 32;
   else if (g.D % 8 == 0) VB = 16;
@@ -223,11 +235,11 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.dv = FastDiv(Dv);
   p.span = g.regions();
   switch (VB) {
-    case 32: return run_copy<32>(p, dir, max_desc, s);
-    case 16: return run_copy<16>(p, dir, max_desc, s);
-    case 8: return run_copy<8>(p, dir, max_desc, s);
-    case 4: return run_copy<4>(p, dir, max_desc, s);
-    default: return run_copy<2>(p, dir, max_desc, s);
+    case 32: return run_copy<32>(p, dir, max_desc, s, chained);
+    case 16: return run_copy<16>(p, dir, max_desc, s, chained);
+    case 8: return run_copy<8>(p, dir, max_desc, s, chained);
+    case 4: return run_copy<4>(p, dir, max_desc, s, chained);
+    default: return run_copy<2>(p, dir, max_desc, s, chained);
   }
 }
 

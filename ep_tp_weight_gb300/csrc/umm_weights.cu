@@ -40,6 +40,7 @@ struct WParams {
 template <int VB, int U, int T>
 __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) {
   using V = typename VecT<VB>::T;
+  griddep_launch_dependents();
   for (uint32_t tile = blockIdx.x; tile < p.tiles_total; tile += gridDim.x) {
     uint32_t r, lt;
     p.tiles_per_region.divmod(tile, r, lt);
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) 
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(ep_addr[u]));
+      griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u]) st_stream(reinterpret_cast<V*>(tp_addr[u]), val[u]);
@@ -107,11 +109,13 @@ __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) 
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(tp_addr[u]));
+      griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u]) st_stream(reinterpret_cast<V*>(ep_addr[u]), val[u]);
     }
   }
+  griddep_wait();
 }
 
 namespace {
@@ -123,10 +127,9 @@ constexpr int kU = 4;
 // is done, keeping more loads in flight (measured on GB300, E=128, H=2048,
 // I=768: 6.35 TB/s persistent with 8 vectors per thread -> 6.95 TB/s).
 template <int VB>
-cudaError_t run(const WParams& p, int ep2tp, cudaStream_t s) {
+cudaError_t run(const WParams& p, int ep2tp, cudaStream_t s, bool chained) {
   if (p.tiles_total == 0) return cudaSuccess;
-  weights_kernel<VB, kU, kT><<<p.tiles_total, kT, 0, s>>>(p, ep2tp);
-  return cudaGetLastError();
+  return launch_chain(weights_kernel<VB, kU, kT>, p.tiles_total, kT, s, chained, p, ep2tp);
 }
 }  // namespace
 
@@ -183,12 +186,12 @@ WParams layer_params(const Geo& g, int layer, int VB) {
   return p;
 }
 
-cudaError_t run_any(const WParams& p, int VB, int ep2tp, cudaStream_t s) {
+cudaError_t run_any(const WParams& p, int VB, int ep2tp, cudaStream_t s, bool chained) {
   switch (VB) {
-    case 16: return run<16>(p, ep2tp, s);
-    case 8: return run<8>(p, ep2tp, s);
-    case 4: return run<4>(p, ep2tp, s);
-    default: return run<2>(p, ep2tp, s);
+    case 16: return run<16>(p, ep2tp, s, chained);
+    case 8: return run<8>(p, ep2tp, s, chained);
+    case 4: return run<4>(p, ep2tp, s, chained);
+    default: return run<2>(p, ep2tp, s, chained);
   }
 }
 
@@ -269,9 +272,9 @@ cudaError_t run_exchange(const Geo& g, int layer, int VB, const uint8_t* stage, 
 
 }  // namespace
 
-cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s) {
+cudaError_t launch_weights(const Geo& g, int ep2tp, int layer, cudaStream_t s, bool chained) {
   const int VB = vec_bytes((uint32_t)g.H, (uint32_t)(g.I / g.P));
-  return run_any(layer_params(g, layer, VB), VB, ep2tp, s);
+  return run_any(layer_params(g, layer, VB), VB, ep2tp, s, chained);
 }
 
 uint64_t weights_stage_bytes(const Geo& g) {
@@ -294,11 +297,11 @@ cudaError_t launch_weights_staged(const Geo& g, int ep2tp, int layer, uint8_t* s
   p.tp_span = Span{stage, stage + weights_stage_bytes(g), g.flags};
   cudaError_t e;
   if (ep2tp) {   // permute into per-peer blocks, then exchange into the TP slots
-    if ((e = run_any(p, VB, 1, s)) != cudaSuccess) return e;
+    if ((e = run_any(p, VB, 1, s, false)) != cudaSuccess) return e;
     e = run_exchange(g, layer, VB, stage, 1, s);
   } else {       // exchange out of the TP slots, then permute into whole experts
     if ((e = run_exchange(g, layer, VB, stage, 0, s)) != cudaSuccess) return e;
-    e = run_any(p, VB, 0, s);
+    e = run_any(p, VB, 0, s, false);
   }
   *launches = 2;
   return e;

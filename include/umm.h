@@ -44,6 +44,11 @@
  *    the workspace; every later validating kernel (KV, placement, request
  *    order, page hand-out) then does nothing until umm_status_sync() reads and
  *    clears them.  Weight reshards cannot fail on the device and ignore them.
+ *  - The per-layer copies of one call (weights, KV, attention) are launched
+ *    as a chain: layer k+1 uses programmatic dependent launch, so its CTAs
+ *    may start, and read slots that no layer of the call writes, while layer
+ *    k drains; each of its stores waits for layer k's grid to complete.  The
+ *    chain is off while per-kernel timing (umm_profile_enable) is on.
  *  - The library never aborts, traps or throws across this ABI.
  *  - A handle is not thread-safe: issue its calls from one host thread, with
  *    the buffer's device current.
@@ -54,6 +59,8 @@
  *    against the vector's alignment.  A failing access is skipped and raises
  *    UMM_FLAG_ACCESS (status UMM_ERR_ACCESS).  The checked build serves tests;
  *    the flag can only come from a library fault, never from caller input.
+ *    A KV layer already started in the chain when the flag is raised still
+ *    runs (it read the flags before the previous layer finished).
  */
 #ifndef UMM_H_
 #define UMM_H_
