@@ -475,14 +475,17 @@ def test_attn_needs_attention_dims():
 @pytest.mark.parametrize("w", [TINY.with_(Hq=4), Workload("switch_mid", P=4, N=3, E=8, H=40, I=24, Hkv=2, D=8, ps=4,
                                                             R=20, len_a=1, len_b=37, slack=3.0, Hq=8)],
                          ids=lambda w: w.name)
-@pytest.mark.parametrize("overlap", [False, True], ids=["serial", "overlap"])
-def test_switch_entry_points_equal_oracle(w, overlap):
+@pytest.mark.parametrize("mode", ["serial", "overlap", "timed"])
+def test_switch_entry_points_equal_oracle(w, mode):
     """umm_switch_ep2tp / umm_switch_tp2ep: weights, attention, request
     order, page hand-out and KV in one call each; the same bytes and metadata
     as the oracle's step-by-step definition, with the weights on the caller's
-    stream or on the handle's side stream (overlap)."""
+    stream or on the handle's side stream (overlap).  Layer copies launch
+    chained (programmatic dependent launch) except under per-kernel timing
+    (timed), where each sits between two events: both give the same bytes."""
     dev = DevUMM(w, seed=17)
-    umm.umm_set_switch_overlap(dev.h, overlap)
+    umm.umm_set_switch_overlap(dev.h, mode == "overlap")
+    umm.umm_profile_enable(dev.h, mode == "timed")
     d, L = dev.d, dev.L
     st = initial_kv_state(w, d, L, seed=3)
     R, maxp = len(st.lens), st.ep_pt.shape[1]
@@ -520,6 +523,10 @@ def test_switch_entry_points_equal_oracle(w, overlap):
         umm.umm_switch_tp2ep(dev.h, R, maxp, i32(st.lens), d_pos, d_tp_pt, i32(ep_free), L["pages_ep"],
                              L["pages_ep"], d_owner, d_local, d_ep_pt)
     assert ei.value.code == umm.UMM_ERR_MODE
+    if mode == "timed":
+        launches = {umm.KIND_NAMES[k]: umm.umm_profile_read(dev.h, k)[0] for k in range(umm.K_COUNT)}
+        for kind in ("weights_ep2tp", "weights_tp2ep", "kv_ep2tp", "kv_tp2ep", "attn_ep2tp", "attn_tp2ep"):
+            assert launches[kind] == d.N, (kind, launches)
     dev.close()
 
 
