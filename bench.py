@@ -172,24 +172,30 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- traffic from committed ncu summary
 
-KERNEL_SOURCES = {"kv_copy_ep2tp": "ep_tp_weight_gb300/csrc/umm_kv.cu",
-                  "kv_copy_tp2ep": "ep_tp_weight_gb300/csrc/umm_kv.cu",
-                  "weights_kernel": "ep_tp_weight_gb300/csrc/umm_weights.cu"}
+_CSRC = "ep_tp_weight_gb300/csrc/"
+KERNEL_SOURCES = {"kv_copy_ep2tp": (_CSRC + "umm_kv.cu", _CSRC + "umm_scan.cuh", _CSRC + "umm_internal.cuh"),
+                  "kv_copy_tp2ep": (_CSRC + "umm_kv.cu", _CSRC + "umm_scan.cuh", _CSRC + "umm_internal.cuh"),
+                  "weights_kernel": (_CSRC + "umm_weights.cu", _CSRC + "umm_internal.cuh")}
 # the ncu capture (small case of the same kernel) each traffic figure comes from
 PROFILE_CASES = {"kv_copy_ep2tp": "kv_p8_2layers_8req_u1k-32k_hkv4_d128",
                  "kv_copy_tp2ep": "kv_p8_2layers_8req_u1k-32k_hkv4_d128",
                  "weights_kernel": "weights_p8_e128_h2048_i768_2layers"}
 
 
-def source_digest(rel: str) -> str:
-    """sha256 (16 hex) of a source file's code: comments and whitespace are
-    dropped, so edits to comments keep a profile valid and code edits do not."""
-    with open(os.path.join(ROOT, rel)) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", "", text)
-    text = re.sub(r"\s+", "", text)
-    return hashlib.sha256(text.encode()).hexdigest()[:16]
+def source_digest(rels) -> str:
+    """sha256 (16 hex) of the code of a kernel's source files (its .cu file and
+    the headers it includes, in order): comments and whitespace are dropped,
+    so edits to comments keep a profile valid and code edits do not."""
+    if isinstance(rels, str):
+        rels = (rels,)
+    code = []
+    for rel in rels:
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code.append(re.sub(r"\s+", "", text))
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 def committed_traffic(kernel: str, units: dict):

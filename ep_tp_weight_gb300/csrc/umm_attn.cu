@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
         const uint8_t* src = ep2tp ? p.base + (uint64_t)q * p.region_stride + p.ep_slot + full_off[u]
                                    : shard + shard_off;
         ok[u] = access_ok<VB>(p.span, src);
-        if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(src));
+        if (ok[u]) val[u] = ld_vec(reinterpret_cast<const V*>(src));
         if (ep2tp) full_off[u] = shard_off;   // from here on: where to store
       }
     }
@@ -88,11 +88,11 @@ __global__ void __launch_bounds__(T) attn_kernel(const AParams p, int ep2tp) {
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
       if (ep2tp) {
-        if (access_ok<VB>(p.span, shard + full_off[u])) st_stream(reinterpret_cast<V*>(shard + full_off[u]), val[u]);
+        if (access_ok<VB>(p.span, shard + full_off[u])) st_vec(reinterpret_cast<V*>(shard + full_off[u]), val[u]);
       } else {
         for (uint32_t r = 0; r < p.P; ++r) {
           uint8_t* const dst = p.base + (uint64_t)r * p.region_stride + p.ep_slot + full_off[u];
-          if (access_ok<VB>(p.span, dst)) st_stream(reinterpret_cast<V*>(dst), val[u]);
+          if (access_ok<VB>(p.span, dst)) st_vec(reinterpret_cast<V*>(dst), val[u]);
         }
       }
     }

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
         p.dv.divmod(rem2, h[u], dvv[u]);
         if (v < nvec && tok[u] < (uint32_t)d.ntok) {
           const uint8_t* const src = src_region + c[u] * p.kv_v_off + src_page + (uint64_t)rem * VB;
-          if (access_ok<VB>(p.span, src)) val[u] = ld_stream(reinterpret_cast<const V*>(src));
+          if (access_ok<VB>(p.span, src)) val[u] = ld_vec(reinterpret_cast<const V*>(src));
           else tok[u] = 0xffffffffu;
         } else {
           tok[u] = 0xffffffffu;
@@ -98,12 +98,12 @@ __global__ void __launch_bounds__(T) kv_copy_ep2tp(const KVParams p) {
           for (uint32_t j = 0; j < p.rep; ++j) {
             const uint32_t q = h[u] * p.rep + j;
             uint8_t* const dst = p.base + (uint64_t)q * p.region_stride + row_off;
-            if (access_ok<VB>(p.span, dst)) st_stream(reinterpret_cast<V*>(dst), val[u]);
+            if (access_ok<VB>(p.span, dst)) st_vec(reinterpret_cast<V*>(dst), val[u]);
           }
         } else {
           const uint32_t q = h[u] / p.h_tp, hl = h[u] - q * p.h_tp;
           uint8_t* const dst = p.base + (uint64_t)q * p.region_stride + row_off + (uint64_t)hl * p.head_bytes;
-          if (access_ok<VB>(p.span, dst)) st_stream(reinterpret_cast<V*>(dst), val[u]);
+          if (access_ok<VB>(p.span, dst)) st_vec(reinterpret_cast<V*>(dst), val[u]);
         }
       }
     }
@@ -156,14 +156,14 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
                                      (uint64_t)dvv * VB;
           ok[u] = access_ok<VB>(p.span, src) &&
                   access_ok<VB>(p.span, dst_region + c[u] * p.kv_v_off + dst_page + (uint64_t)rem * VB);
-          if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(src));
+          if (ok[u]) val[u] = ld_vec(reinterpret_cast<const V*>(src));
         }
       }
       griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (ok[u])
-          st_stream(reinterpret_cast<V*>(dst_region + c[u] * p.kv_v_off + dst_page + (uint64_t)rem_[u] * VB),
+          st_vec(reinterpret_cast<V*>(dst_region + c[u] * p.kv_v_off + dst_page + (uint64_t)rem_[u] * VB),
                  val[u]);
     }
   }

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) kv_stage_gather(const SParams p, int dir)
       }
       uint8_t* const dst = p.send + (((uint64_t)slot * T + t0 + tok) * p.tp_row) + (uint64_t)cv * VB;
       if (access_ok<VB>(p.regions, src) && access_ok<VB>(p.staging, dst))
-        st_stream(reinterpret_cast<V*>(dst), ld_stream(reinterpret_cast<const V*>(src)));
+        st_vec(reinterpret_cast<V*>(dst), ld_vec(reinterpret_cast<const V*>(src)));
     }
   }
 }
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(256) kv_stage_exchange(const SParams p, int di
   for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += (uint64_t)gridDim.x * blockDim.x)
     if (access_ok<VB>(p.staging, reinterpret_cast<V*>(p.send) + v) &&
         access_ok<VB>(p.staging, reinterpret_cast<V*>(p.recv) + v))
-      st_stream(reinterpret_cast<V*>(p.recv) + v, ld_stream(reinterpret_cast<const V*>(p.send) + v));
+      st_vec(reinterpret_cast<V*>(p.recv) + v, ld_vec(reinterpret_cast<const V*>(p.send) + v));
 }
 
 // stage 3, scatter: recv -> target pages (EP->TP: every TP rank's page;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(256) kv_stage_scatter(const SParams p, int dir
               ((uint64_t)d.dst_page * p.ps + tok) * p.ep_row + (uint64_t)qg * p.h_tp * p.head_bytes +
               (uint64_t)cv * VB;
       if (access_ok<VB>(p.staging, src) && access_ok<VB>(p.regions, dst))
-        st_stream(reinterpret_cast<V*>(dst), ld_stream(src));
+        st_vec(reinterpret_cast<V*>(dst), ld_vec(src));
     }
   }
 }

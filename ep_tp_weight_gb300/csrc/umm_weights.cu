@@ -100,19 +100,19 @@ __global__ void __launch_bounds__(T) weights_kernel(const WParams p, int ep2tp) 
     if (ep2tp) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(ep_addr[u]));
+        if (ok[u]) val[u] = ld_vec(reinterpret_cast<const V*>(ep_addr[u]));
       griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ok[u]) st_stream(reinterpret_cast<V*>(tp_addr[u]), val[u]);
+        if (ok[u]) st_vec(reinterpret_cast<V*>(tp_addr[u]), val[u]);
     } else {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>(tp_addr[u]));
+        if (ok[u]) val[u] = ld_vec(reinterpret_cast<const V*>(tp_addr[u]));
       griddep_wait();
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ok[u]) st_stream(reinterpret_cast<V*>(ep_addr[u]), val[u]);
+        if (ok[u]) st_vec(reinterpret_cast<V*>(ep_addr[u]), val[u]);
     }
   }
   griddep_wait();
@@ -230,12 +230,12 @@ __global__ void __launch_bounds__(T) exchange_kernel(const XParams p, int to_tp)
     for (int u = 0; u < U; ++u) {
       const uint64_t o = off0 + (uint64_t)(u * T + threadIdx.x) * VB;
       ok[u] = o < seg && access_ok<VB>(p.stage_span, st + o) && access_ok<VB>(p.region_span, tp + o);
-      if (ok[u]) val[u] = ld_stream(reinterpret_cast<const V*>((to_tp ? st : tp) + o));
+      if (ok[u]) val[u] = ld_vec(reinterpret_cast<const V*>((to_tp ? st : tp) + o));
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint64_t o = off0 + (uint64_t)(u * T + threadIdx.x) * VB;
-      if (ok[u]) st_stream(reinterpret_cast<V*>(const_cast<uint8_t*>(to_tp ? tp : st) + o), val[u]);
+      if (ok[u]) st_vec(reinterpret_cast<V*>(const_cast<uint8_t*>(to_tp ? tp : st) + o), val[u]);
     }
   }
 }

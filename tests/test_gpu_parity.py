@@ -530,12 +530,14 @@ def test_switch_entry_points_equal_oracle(w, mode):
     dev.close()
 
 
-def test_many_round_trips_stay_exact():
+@pytest.mark.parametrize("overlap", [False, True], ids=["serial", "overlap"])
+def test_many_round_trips_stay_exact(overlap):
     """40 EP->TP->EP round trips through umm_switch_* on one handle, each with
     fresh free lists, the KV pool two-thirds full so that the copies walk it
     through the call-tagged TP-page schedule (stale entries of earlier calls
     must be ignored), and the status read only at the end: equal to the
-    oracle step for step."""
+    oracle step for step.  The layer copies launch chained; with overlap the
+    weight chains run on the side stream beside the KV chains."""
     w = Workload("many_trips", P=4, N=2, E=8, H=32, I=16, Hkv=2, D=16, ps=4, R=24, len_a=1, len_b=30,
                  slack=1.5, Hq=8)
     lens = w.lengths().copy()
@@ -545,6 +547,7 @@ def test_many_round_trips_stay_exact():
     m = w.Hkv // w.h_tp
     ptp = (int(1.5 * used) + m - 1) // m * m
     dev = DevUMM(w, seed=29, pages_tp=ptp, max_requests=len(lens), max_pages=ptp)
+    umm.umm_set_switch_overlap(dev.h, overlap)
     d, L = dev.d, dev.L
     R, P = len(lens), d.P
     owner, _, _ = oracle.place(P, lens)
