@@ -3,8 +3,11 @@
 Every function here has the name of its C entry point in include/umm.h and
 does nothing but convert arguments: torch tensors become device pointers,
 torch streams become cudaStream_t handles, non-zero status codes become
-``UmmError``.  All work runs in the library's CUDA kernels.  Importing this
-module fails loudly when libumm.so has not been built.
+``UmmError``.  Tensor arguments are checked first (a contiguous CUDA tensor
+of int32, or bytes for buffers, large enough for the sizes passed), so a host
+tensor or a short table is refused instead of reaching a kernel.  All work
+runs in the library's CUDA kernels.  Importing this module fails loudly when
+libumm.so has not been built.
 """
 from __future__ import annotations
 
@@ -177,6 +180,35 @@ def _ptr(x):
     return int(x) or None
 
 
+def _arr(x, n: int, where: str, what: str):
+    """Device pointer of a caller array that the call reads or writes as n
+    int32 elements.  A tensor must be a contiguous int32 CUDA tensor with at
+    least n elements; anything else raises UmmError(UMM_ERR_INVALID_ARG) before
+    the library is called, so a host tensor or a short table never reaches a
+    kernel.  A raw int address is passed through: its size is the caller's
+    responsibility, as in C.  None stays NULL."""
+    if x is None or not hasattr(x, "data_ptr"):
+        return _ptr(x)
+    dev = getattr(x, "device", None)
+    if (dev is None or dev.type != "cuda" or str(x.dtype) != "torch.int32" or not x.is_contiguous()
+            or x.numel() < n):
+        raise UmmError(UMM_ERR_INVALID_ARG, f"{where} ({what}: a contiguous int32 CUDA tensor of at least "
+                                            f"{n} elements is required)")
+    return x.data_ptr() or None
+
+
+def _buf(x, nbytes: int, where: str, what: str):
+    """Device pointer of a caller byte buffer of at least nbytes (a contiguous
+    CUDA tensor of any dtype, or a raw int address); as _arr."""
+    if x is None or not hasattr(x, "data_ptr"):
+        return _ptr(x)
+    dev = getattr(x, "device", None)
+    if dev is None or dev.type != "cuda" or not x.is_contiguous() or x.numel() * x.element_size() < nbytes:
+        raise UmmError(UMM_ERR_INVALID_ARG, f"{where} ({what}: a contiguous CUDA tensor of at least "
+                                            f"{nbytes} bytes is required)")
+    return x.data_ptr() or None
+
+
 def _stream(s):
     if s is None:
         return None
@@ -207,7 +239,8 @@ def umm_layout_for_dims(dims: UmmDims) -> dict:
 
 def umm_create(dims: UmmDims, d_base, nbytes: int) -> int:
     h = ctypes.c_void_p()
-    _ck(_lib.umm_create(ctypes.byref(dims), _ptr(d_base), int(nbytes), ctypes.byref(h)), "umm_create")
+    base = _buf(d_base, int(nbytes), "umm_create", "d_base")
+    _ck(_lib.umm_create(ctypes.byref(dims), base, int(nbytes), ctypes.byref(h)), "umm_create")
     return h.value
 
 
@@ -246,13 +279,15 @@ def umm_weights_stage_bytes(h: int) -> int:
 
 
 def reshard_weights_ep2tp_staged(h: int, stage, stage_bytes: int, stream=None) -> None:
-    _ck(_lib.reshard_weights_ep2tp_staged(h, _ptr(stage), int(stage_bytes), _stream(stream)),
-        "reshard_weights_ep2tp_staged")
+    w = "reshard_weights_ep2tp_staged"
+    _ck(_lib.reshard_weights_ep2tp_staged(h, _buf(stage, int(stage_bytes), w, "stage"), int(stage_bytes),
+                                          _stream(stream)), w)
 
 
 def reshard_weights_tp2ep_staged(h: int, stage, stage_bytes: int, stream=None) -> None:
-    _ck(_lib.reshard_weights_tp2ep_staged(h, _ptr(stage), int(stage_bytes), _stream(stream)),
-        "reshard_weights_tp2ep_staged")
+    w = "reshard_weights_tp2ep_staged"
+    _ck(_lib.reshard_weights_tp2ep_staged(h, _buf(stage, int(stage_bytes), w, "stage"), int(stage_bytes),
+                                          _stream(stream)), w)
 
 
 def umm_kv_stage_bytes(h: int) -> int:
@@ -263,16 +298,20 @@ def umm_kv_stage_bytes(h: int) -> int:
 
 def reshard_kv_ep2tp_staged(h: int, stage, stage_bytes: int, R: int, max_pages_per_req: int, seq_lens,
                             ep_owner, ep_page_table, tp_page_table, stream=None) -> None:
-    _ck(_lib.reshard_kv_ep2tp_staged(h, _ptr(stage), int(stage_bytes), R, max_pages_per_req, _ptr(seq_lens),
-                                     _ptr(ep_owner), _ptr(ep_page_table), _ptr(tp_page_table), _stream(stream)),
-        "reshard_kv_ep2tp_staged")
+    w, n, t = "reshard_kv_ep2tp_staged", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    _ck(_lib.reshard_kv_ep2tp_staged(h, _buf(stage, int(stage_bytes), w, "stage"), int(stage_bytes), R,
+                                     max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
+                                     _arr(ep_owner, n, w, "ep_owner"), _arr(ep_page_table, t, w, "ep_page_table"),
+                                     _arr(tp_page_table, t, w, "tp_page_table"), _stream(stream)), w)
 
 
 def reshard_kv_tp2ep_staged(h: int, stage, stage_bytes: int, R: int, max_pages_per_req: int, seq_lens,
                             ep_owner, ep_page_table, tp_page_table, stream=None) -> None:
-    _ck(_lib.reshard_kv_tp2ep_staged(h, _ptr(stage), int(stage_bytes), R, max_pages_per_req, _ptr(seq_lens),
-                                     _ptr(ep_owner), _ptr(ep_page_table), _ptr(tp_page_table), _stream(stream)),
-        "reshard_kv_tp2ep_staged")
+    w, n, t = "reshard_kv_tp2ep_staged", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    _ck(_lib.reshard_kv_tp2ep_staged(h, _buf(stage, int(stage_bytes), w, "stage"), int(stage_bytes), R,
+                                     max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
+                                     _arr(ep_owner, n, w, "ep_owner"), _arr(ep_page_table, t, w, "ep_page_table"),
+                                     _arr(tp_page_table, t, w, "tp_page_table"), _stream(stream)), w)
 
 
 def reshard_attn_ep2tp(h: int, stream=None) -> None:
@@ -294,55 +333,77 @@ def umm_set_attn_mode(h: int, mode: int) -> None:
 
 
 def gather_requests_ep2tp(h: int, R: int, ep_owner, tp_pos, stream=None) -> None:
-    _ck(_lib.gather_requests_ep2tp(h, R, _ptr(ep_owner), _ptr(tp_pos), _stream(stream)),
-        "gather_requests_ep2tp")
+    w, n = "gather_requests_ep2tp", max(R, 0)
+    _ck(_lib.gather_requests_ep2tp(h, R, _arr(ep_owner, n, w, "ep_owner"), _arr(tp_pos, n, w, "tp_pos"),
+                                   _stream(stream)), w)
 
 
 def place_requests_tp2ep(h: int, R: int, seq_lens, list_pos, owner, local_pos, stream=None) -> None:
-    _ck(_lib.place_requests_tp2ep(h, R, _ptr(seq_lens), _ptr(list_pos), _ptr(owner), _ptr(local_pos),
-                                  _stream(stream)), "place_requests_tp2ep")
+    w, n = "place_requests_tp2ep", max(R, 0)
+    _ck(_lib.place_requests_tp2ep(h, R, _arr(seq_lens, n, w, "seq_lens"), _arr(list_pos, n, w, "list_pos"),
+                                  _arr(owner, n, w, "owner"), _arr(local_pos, n, w, "local_pos"),
+                                  _stream(stream)), w)
 
 
 def place_requests_tp2ep_noalloc(P: int, R: int, seq_lens, list_pos, owner, local_pos, status=None,
                                  stream=None) -> None:
     """place_requests_tp2ep without a handle and without any allocation (for
     callers that cannot allocate device memory); R <= 16384."""
-    _ck(_lib.place_requests_tp2ep_noalloc(P, R, _ptr(seq_lens), _ptr(list_pos), _ptr(owner), _ptr(local_pos),
-                                          _ptr(status), _stream(stream)), "place_requests_tp2ep_noalloc")
+    w, n = "place_requests_tp2ep_noalloc", max(R, 0)
+    _ck(_lib.place_requests_tp2ep_noalloc(P, R, _arr(seq_lens, n, w, "seq_lens"), _arr(list_pos, n, w, "list_pos"),
+                                          _arr(owner, n, w, "owner"), _arr(local_pos, n, w, "local_pos"),
+                                          _arr(status, 1, w, "status"), _stream(stream)), w)
 
 
 def umm_assign_pages(h: int, npools: int, R: int, seq_lens, pool, key, free_pages, free_stride: int,
                      free_count: int, page_table, max_pages_per_req: int, stream=None) -> None:
-    _ck(_lib.umm_assign_pages(h, npools, R, _ptr(seq_lens), _ptr(pool), _ptr(key), _ptr(free_pages),
-                              int(free_stride), int(free_count), _ptr(page_table), int(max_pages_per_req),
-                              _stream(stream)), "umm_assign_pages")
+    w, n = "umm_assign_pages", max(R, 0)
+    nfree = max(npools - 1, 0) * max(int(free_stride), 0) + max(int(free_count), 0)
+    _ck(_lib.umm_assign_pages(h, npools, R, _arr(seq_lens, n, w, "seq_lens"), _arr(pool, n, w, "pool"),
+                              _arr(key, n, w, "key"), _arr(free_pages, nfree, w, "free_pages"),
+                              int(free_stride), int(free_count),
+                              _arr(page_table, n * max(int(max_pages_per_req), 0), w, "page_table"),
+                              int(max_pages_per_req), _stream(stream)), w)
 
 
 def reshard_kv_ep2tp(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner, ep_page_table,
                      tp_page_table, stream=None) -> None:
-    _ck(_lib.reshard_kv_ep2tp(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
-                              _ptr(tp_page_table), _stream(stream)), "reshard_kv_ep2tp")
+    w, n, t = "reshard_kv_ep2tp", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    _ck(_lib.reshard_kv_ep2tp(h, R, max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
+                              _arr(ep_owner, n, w, "ep_owner"), _arr(ep_page_table, t, w, "ep_page_table"),
+                              _arr(tp_page_table, t, w, "tp_page_table"), _stream(stream)), w)
 
 
 def reshard_kv_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner, ep_page_table,
                      tp_page_table, stream=None) -> None:
-    _ck(_lib.reshard_kv_tp2ep(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
-                              _ptr(tp_page_table), _stream(stream)), "reshard_kv_tp2ep")
+    w, n, t = "reshard_kv_tp2ep", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    _ck(_lib.reshard_kv_tp2ep(h, R, max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
+                              _arr(ep_owner, n, w, "ep_owner"), _arr(ep_page_table, t, w, "ep_page_table"),
+                              _arr(tp_page_table, t, w, "tp_page_table"), _stream(stream)), w)
 
 
 def umm_switch_ep2tp(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner, ep_page_table, tp_free_pages,
                      tp_free_count: int, tp_pos, tp_page_table, stream=None) -> None:
-    _ck(_lib.umm_switch_ep2tp(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(ep_owner), _ptr(ep_page_table),
-                              _ptr(tp_free_pages), int(tp_free_count), _ptr(tp_pos), _ptr(tp_page_table),
-                              _stream(stream)), "umm_switch_ep2tp")
+    w, n, t = "umm_switch_ep2tp", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    _ck(_lib.umm_switch_ep2tp(h, R, max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
+                              _arr(ep_owner, n, w, "ep_owner"), _arr(ep_page_table, t, w, "ep_page_table"),
+                              _arr(tp_free_pages, max(int(tp_free_count), 0), w, "tp_free_pages"),
+                              int(tp_free_count), _arr(tp_pos, n, w, "tp_pos"),
+                              _arr(tp_page_table, t, w, "tp_page_table"), _stream(stream)), w)
 
 
 def umm_switch_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, tp_pos, tp_page_table, ep_free_pages,
                      ep_free_stride: int, ep_free_count: int, ep_owner, local_pos, ep_page_table,
                      stream=None) -> None:
-    _ck(_lib.umm_switch_tp2ep(h, R, max_pages_per_req, _ptr(seq_lens), _ptr(tp_pos), _ptr(tp_page_table),
-                              _ptr(ep_free_pages), int(ep_free_stride), int(ep_free_count), _ptr(ep_owner),
-                              _ptr(local_pos), _ptr(ep_page_table), _stream(stream)), "umm_switch_tp2ep")
+    # the number of pools (P) is not known here: the free lists are checked
+    # for one pool's count; the library reads (P-1) * stride + count entries
+    w, n, t = "umm_switch_tp2ep", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    _ck(_lib.umm_switch_tp2ep(h, R, max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
+                              _arr(tp_pos, n, w, "tp_pos"), _arr(tp_page_table, t, w, "tp_page_table"),
+                              _arr(ep_free_pages, max(int(ep_free_count), 0), w, "ep_free_pages"),
+                              int(ep_free_stride), int(ep_free_count), _arr(ep_owner, n, w, "ep_owner"),
+                              _arr(local_pos, n, w, "local_pos"), _arr(ep_page_table, t, w, "ep_page_table"),
+                              _stream(stream)), w)
 
 
 def umm_set_switch_overlap(h: int, enable: bool = True) -> None:

@@ -184,3 +184,87 @@ def test_c_program_uses_the_abi(umm, tmp_path):
     assert got["strerror_capacity"] == umm.strerror(umm.UMM_ERR_CAPACITY)
     assert (int(got["policy_last_decision"]), int(got["policy_mode"]), int(got["policy_switches"])) == \
         (umm.POLICY_TO_EP, umm.UMM_MODE_EP, 1)
+
+
+class _FakeDevice:
+    def __init__(self, kind):
+        self.type = kind
+
+
+class _FakeTensor:
+    """Just enough of a tensor for the binding's argument checks."""
+
+    def __init__(self, n, dtype="torch.int32", kind="cuda", contiguous=True, itemsize=4):
+        self.n, self.dtype, self.device, self.contig, self.itemsize = n, dtype, _FakeDevice(kind), contiguous, itemsize
+
+    def data_ptr(self):
+        return 0x7f0000000000
+
+    def numel(self):
+        return self.n
+
+    def element_size(self):
+        return self.itemsize
+
+    def is_contiguous(self):
+        return self.contig
+
+
+class _SpyLib:
+    """Stands in for libumm: records which entry points were reached."""
+
+    def __init__(self):
+        self.calls = []
+
+    def __getattr__(self, name):
+        if name == "umm_strerror":
+            return lambda code: b"status text"
+
+        def call(*args):
+            self.calls.append(name)
+            return 0
+        return call
+
+
+def test_binding_refuses_arrays_that_cannot_be_the_kernels_input(umm, monkeypatch):
+    """A host tensor, another dtype, a strided view or a table shorter than
+    R x max_pages_per_req is refused with UMM_ERR_INVALID_ARG before the library
+    is called, so it never reaches a kernel as a device pointer; a contiguous
+    int32 CUDA array of the right size, or a raw address, goes through."""
+    import torch
+    spy = _SpyLib()
+    monkeypatch.setattr(umm, "_lib", spy)
+    R, maxp = 6, 3
+    ok_vec, ok_tab = _FakeTensor(R), _FakeTensor(R * maxp)
+
+    def kv(seq_lens=ok_vec, ep_pt=ok_tab):
+        umm.reshard_kv_ep2tp(0x1, R, maxp, seq_lens, ok_vec, ep_pt, ok_tab)
+
+    kv()
+    assert spy.calls == ["reshard_kv_ep2tp"]
+    bad = [dict(seq_lens=torch.zeros(R, dtype=torch.int32)),          # host memory
+           dict(seq_lens=_FakeTensor(R, dtype="torch.int64")),        # another dtype
+           dict(seq_lens=_FakeTensor(R, contiguous=False)),          # strided view
+           dict(seq_lens=_FakeTensor(R - 1)),                        # too short
+           dict(ep_pt=_FakeTensor(R * maxp - 1))]                    # table too short
+    for kw in bad:
+        with pytest.raises(umm.UmmError) as ei:
+            kv(**kw)
+        assert ei.value.code == umm.UMM_ERR_INVALID_ARG, kw
+    assert spy.calls == ["reshard_kv_ep2tp"]
+    umm.reshard_kv_ep2tp(0x1, R, maxp, 0x1000, 0x2000, 0x3000, 0x4000)   # raw addresses: the caller's word
+    umm.reshard_kv_ep2tp(0x1, 0, maxp, None, None, None, None)           # R = 0: nothing to check
+    assert spy.calls == ["reshard_kv_ep2tp"] * 3
+    with pytest.raises(umm.UmmError) as ei:                              # free list shorter than its count
+        umm.umm_switch_ep2tp(0x1, R, maxp, ok_vec, ok_vec, ok_tab, _FakeTensor(9), 10, ok_vec, ok_tab)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    with pytest.raises(umm.UmmError) as ei:                              # pools 0..2 need 2*stride + count entries
+        umm.umm_assign_pages(0x1, 3, R, ok_vec, ok_vec, ok_vec, _FakeTensor(2 * 8 + 4), 8, 5, ok_tab, maxp)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    umm.umm_assign_pages(0x1, 3, R, ok_vec, ok_vec, ok_vec, _FakeTensor(2 * 8 + 5), 8, 5, ok_tab, maxp)
+    with pytest.raises(umm.UmmError) as ei:                              # buffer smaller than claimed
+        umm.umm_create(lib_dims(umm, TINY), _FakeTensor(1000, dtype="torch.uint8", itemsize=1), 1001)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    with pytest.raises(umm.UmmError):
+        umm.umm_create(lib_dims(umm, TINY), torch.zeros(64, dtype=torch.uint8), 64)
+    assert spy.calls == ["reshard_kv_ep2tp"] * 3 + ["umm_assign_pages"]
