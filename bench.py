@@ -66,6 +66,11 @@ def parse():
     ap.add_argument("--phase-sweep", action="store_true",
                     help="instead of the benchmark line: the full-switch shape at several request counts, "
                          "one JSON line each with ms per phase (weights, request metadata, descriptor pass, KV)")
+    ap.add_argument("--no-ceilings", action="store_true",
+                    help="skip the read:write-mix ceilings measured after the timed region")
+    ap.add_argument("--ceilings", action="store_true",
+                    help="instead of the benchmark line: the HBM rate a plain streaming copy reaches for the "
+                         "read:write mix of each reshard kernel, one JSON line per mix")
     args = ap.parse_args()
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be at least 1 and --warmup at least 0")
@@ -658,6 +663,40 @@ def phase_sweep(args):
         print(json.dumps(line), flush=True)
 
 
+# the read:write mix of each kernel kind (ep_tp_weight_gb300/csrc/ceiling)
+MIX_OF_KIND = {"weights_ep2tp": "1R1W sequential", "weights_tp2ep": "1R1W sequential",
+               "kv_ep2tp": "1R2W shuffled reads", "kv_tp2ep": "1R1W shuffled writes",
+               "attn_ep2tp": "1R1W sequential", "attn_tp2ep": "1R8W sequential"}
+
+
+def run_ceilings(timeout_s: float = 180.0) -> list[dict]:
+    """Runs the read:write-mix ceiling program (a plain streaming copy for
+    each reshard kernel's access pattern, 8 GiB buffers) on this process's
+    GPU; its JSON lines, or [] when it cannot be built or run here."""
+    try:
+        from ep_tp_weight_gb300 import build as umm_build
+        exe = umm_build.build_ceiling()
+        env = dict(os.environ)
+        env.setdefault("CUDA_VISIBLE_DEVICES", os.environ.get("LOCAL_RANK", "0"))
+        out = subprocess.run([exe, "8"], capture_output=True, text=True, timeout=timeout_s, check=True,
+                             env=env).stdout
+    except (OSError, subprocess.SubprocessError):
+        return []
+    return [json.loads(ln) for ln in out.splitlines() if ln.startswith("{")]
+
+
+def ceilings():
+    """`--ceilings`: the read:write-mix ceilings on this GPU, one JSON line
+    each, then the clocks seen while they ran."""
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) as clk:
+        rows = run_ceilings(timeout_s=600.0)
+    if not rows:
+        raise RuntimeError("the ceiling program could not be built or run")
+    for row in rows:
+        print(json.dumps(row), flush=True)
+    print(json.dumps({"ceilings_clocks": clk.summary()}), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -697,6 +736,10 @@ def main():
         if rank == 0:
             phase_sweep(args)
         return
+    if args.ceilings:
+        if rank == 0:
+            ceilings()
+        return
 
     if world > 1:
         import torch.distributed as dist
@@ -734,6 +777,19 @@ def main():
             gbs = b[key] / (per_kind[k]["ms_per_launch"] / 1e3) / 1e9
             per_kind[k]["GB_s"] = round(gbs, 1)
             per_kind[k]["frac_of_peak"] = round(gbs / peak, 4)
+    # the same kernels against a plain streaming copy of their own read:write
+    # mix, measured on this GPU after the timed region (context beside peak)
+    mix = None
+    if not args.no_ceilings:
+        ceil = {row["ceiling"]: row["GB_s"] for row in run_ceilings()}
+        for k, v in per_kind.items():
+            if "GB_s" in v and MIX_OF_KIND.get(k) in ceil:
+                v["mix_ceiling_GB_s"] = ceil[MIX_OF_KIND[k]]
+                v["frac_of_mix_ceiling"] = round(v["GB_s"] / ceil[MIX_OF_KIND[k]], 4)
+        if MIX_OF_KIND.get(dom) in ceil:
+            c = ceil[MIX_OF_KIND[dom]]
+            mix = {"mix": MIX_OF_KIND[dom], "GB_s": c, "frac": round(achieved / c, 4),
+                   "source": "bench.py --ceilings program, same GPU, after the timed region"}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -750,7 +806,8 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} copy GB/s (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": per_launch_bytes},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": per_launch_bytes,
+                     "mix_ceiling": mix},
         "cuda_graph": r["graph"],
         "staged_comparison": None if r["staged"] is None else dict(
             r["staged"], fused_speedup=round(r["staged"]["ms_per_step"] / ms_step, 3)),

@@ -62,6 +62,21 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     return lib
 
 
+CEILING_SRC = os.path.join(CSRC, "ceiling", "mix_ceiling.cu")
+CEILING_EXE = os.path.join(ROOT, "_build", "mix_ceiling")
+
+
+def build_ceiling(force: bool = False) -> str:
+    """Compile the read:write-mix ceiling program (a standalone executable,
+    not part of libumm) for `bench.py --ceilings`."""
+    if force or not os.path.exists(CEILING_EXE) or os.path.getmtime(CEILING_SRC) > os.path.getmtime(CEILING_EXE):
+        os.makedirs(os.path.dirname(CEILING_EXE), exist_ok=True)
+        tmp = CEILING_EXE + f".tmp{os.getpid()}"
+        subprocess.check_call(["nvcc", *ARCH, "-O3", "-std=c++17", "-o", tmp, CEILING_SRC])
+        os.replace(tmp, CEILING_EXE)
+    return CEILING_EXE
+
+
 def build_all(force: bool = False) -> None:
     """Both libraries, compiled side by side."""
     with ThreadPoolExecutor(max_workers=2) as ex:

@@ -1,0 +1,153 @@
+// Ceilings of HBM read:write mixes on one GPU: what a plain streaming copy
+// reaches for the access pattern of each reshard kernel, so that a kernel's
+// rate can be read against the mix it must move rather than against a 1:1
+// copy.  A standalone program (not part of libumm), built and run by
+// `python bench.py --ceilings`; one JSON line per case on stdout.
+//
+// Every case moves 16 KiB per CTA (256 threads x 2 x 32-byte vectors), one
+// CTA per chunk, over buffers of 8 GiB each by default (64x the L2), with the
+// default cache policy:
+//   read sequential / shuffled: CTA b reads source chunk b, or chunk perm[b]
+//   (a fixed random permutation of the chunks: scattered 16 KiB pages);
+//   write sequential / shuffled: likewise for the destination chunk;
+//   nd destinations: the chunk is stored to nd buffers (replicas).
+// Mapping to the reshard kernels: weights and attention EP->TP = 1 read,
+// 1 write, sequential; KV EP->TP = shuffled reads, 2 writes (two replicas of
+// each head); KV TP->EP = sequential reads, shuffled writes; attention
+// TP->EP = 1 read, 8 writes (all-gather into every rank's full copy).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <random>
+#include <vector>
+
+namespace {
+
+struct alignas(32) u256 {
+  uint32_t w[8];
+};
+
+__device__ __forceinline__ u256 ld32(const u256* p) {
+  u256 v;
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                 "=r"(v.w[6]), "=r"(v.w[7])
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st32(u256* p, const u256& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :
+               : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]),
+                 "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
+}
+
+constexpr int kT = 256, kU = 2, kMaxDst = 8;
+constexpr size_t kChunkVec = (size_t)kT * kU;   // 32-byte vectors per chunk
+constexpr size_t kChunk = kChunkVec * 32;       // 16 KiB
+
+struct Dsts {
+  u256* d[kMaxDst];
+};
+
+__global__ void __launch_bounds__(kT) mix_copy(const u256* src, Dsts dst, int nd, const uint32_t* rperm,
+                                               const uint32_t* wperm, uint32_t nchunks) {
+  const uint32_t b = blockIdx.x;
+  if (b >= nchunks) return;
+  const uint32_t rc = rperm ? rperm[b] : b;
+  const uint32_t wc = wperm ? wperm[b] : b;
+  const u256* s = src + (size_t)rc * kChunkVec;
+  u256 v[kU];
+#pragma unroll
+  for (int u = 0; u < kU; ++u) v[u] = ld32(s + threadIdx.x + u * kT);
+#pragma unroll
+  for (int k = 0; k < kMaxDst; ++k) {
+    if (k < nd) {
+      u256* o = dst.d[k] + (size_t)wc * kChunkVec;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) st32(o + threadIdx.x + u * kT, v[u]);
+    }
+  }
+}
+
+struct Case {
+  const char* name;
+  const char* kernels;   // reshard kernels with this pattern
+  int nd;
+  bool shuffled_reads, shuffled_writes;
+};
+
+}  // namespace
+
+#define CK(x)                                                                        \
+  do {                                                                               \
+    cudaError_t e_ = (x);                                                            \
+    if (e_ != cudaSuccess) {                                                         \
+      std::fprintf(stderr, "CUDA error %s at line %d\n", cudaGetErrorString(e_), __LINE__); \
+      return 1;                                                                      \
+    }                                                                                \
+  } while (0)
+
+int main(int argc, char** argv) {
+  // GiB per buffer (1..16, default 8): nine buffers are allocated
+  const int gib = argc > 1 ? std::max(1, std::min(16, std::atoi(argv[1]))) : 8;
+  const size_t S = (size_t)gib << 30;
+  const uint32_t n = (uint32_t)(S / kChunk);
+  u256* src = nullptr;
+  Dsts dst{};
+  uint32_t *rperm = nullptr, *wperm = nullptr;
+  CK(cudaMalloc(&src, S));
+  CK(cudaMemset(src, 0x5a, S));
+  for (int k = 0; k < kMaxDst; ++k) {
+    CK(cudaMalloc(&dst.d[k], S));
+    CK(cudaMemset(dst.d[k], 0, S));
+  }
+  std::vector<uint32_t> p1(n), p2(n);
+  for (uint32_t i = 0; i < n; ++i) p1[i] = p2[i] = i;
+  std::mt19937_64 rng(20251);
+  std::shuffle(p1.begin(), p1.end(), rng);
+  std::shuffle(p2.begin(), p2.end(), rng);
+  CK(cudaMalloc(&rperm, (size_t)n * 4));
+  CK(cudaMalloc(&wperm, (size_t)n * 4));
+  CK(cudaMemcpy(rperm, p1.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(wperm, p2.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  const Case cases[] = {
+      {"1R1W sequential", "weights_kernel, attn_kernel EP->TP", 1, false, false},
+      {"1R1W shuffled reads", "", 1, true, false},
+      {"1R1W shuffled writes", "kv_copy_tp2ep", 1, false, true},
+      {"1R2W sequential", "", 2, false, false},
+      {"1R2W shuffled reads", "kv_copy_ep2tp", 2, true, false},
+      {"1R8W sequential", "attn_kernel TP->EP", 8, false, false},
+  };
+  const int reps = 10;
+  for (const Case& c : cases) {
+    const uint32_t* rp = c.shuffled_reads ? rperm : nullptr;
+    const uint32_t* wp = c.shuffled_writes ? wperm : nullptr;
+    for (int w = 0; w < 3; ++w) mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
+    CK(cudaGetLastError());
+    CK(cudaDeviceSynchronize());
+    CK(cudaEventRecord(e0));
+    for (int r = 0; r < reps; ++r) mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
+    CK(cudaEventRecord(e1));
+    CK(cudaEventSynchronize(e1));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, e0, e1));
+    const double per = ms / reps, bytes = (double)S * (1 + c.nd);
+    std::printf("{\"ceiling\": \"%s\", \"kernels\": \"%s\", \"read_bytes\": %zu, \"write_bytes\": %zu, "
+                "\"ms_per_launch\": %.4f, \"GB_s\": %.1f}\n",
+                c.name, c.kernels, S, S * (size_t)c.nd, per, bytes / (per * 1e-3) / 1e9);
+  }
+  for (int k = 0; k < kMaxDst; ++k) CK(cudaFree(dst.d[k]));
+  CK(cudaFree(src));
+  CK(cudaFree(rperm));
+  CK(cudaFree(wperm));
+  return 0;
+}

@@ -111,3 +111,14 @@ def test_algorithmic_bytes_equal_elements_the_oracle_moves(w):
     wr2 = 2 * _nonzero_u16(buf, [(kvslot(L, r, 1, 0), L["kvslot_stride"]) for r in range(w.P)])
     assert 2 * wr2 == b["kv_tp2ep_per_layer"]               # read once, written once
     assert b["tokens"] == int(lens.sum())
+
+
+def test_ceiling_program_compiles():
+    """The read:write-mix ceiling program behind `bench.py --ceilings` builds
+    for sm_103a (nvcc cross-compiles here; it runs only on a GPU)."""
+    import shutil
+    if shutil.which("nvcc") is None:
+        pytest.skip("nvcc not on PATH")
+    from ep_tp_weight_gb300 import build as umm_build
+    exe = umm_build.build_ceiling()
+    assert os.path.exists(exe) and os.access(exe, os.X_OK)
