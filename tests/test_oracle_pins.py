@@ -33,7 +33,7 @@ SMALL_KV = Workload("kv_small", P=4, N=3, Hkv=2, D=8, ps=4, R=9, len_kind="unifo
 
 # ----------------------------------------------------------------------------- layout
 
-@pytest.mark.parametrize("w", [TINY, SMALL_W, SMALL_KV, TINY.with_(Hkv=4, P=2, E=4)])
+@pytest.mark.parametrize("w", [TINY, SMALL_W, SMALL_KV, TINY.with_(Hkv=4, P=2, E=4), TINY.with_(Hq=4)])
 def test_layout_parts_disjoint_and_aligned(w):
     d = dims_of(w)
     L = oracle.layout(d)
@@ -52,7 +52,14 @@ def test_layout_parts_disjoint_and_aligned(w):
         assert L["kv_v_off"] >= half_tp and L["kv_v_off"] % 256 == 0
         assert L["kvslot_stride"] >= L["kv_v_off"] + half_tp
     assert L["kvslots_off"] == (d.N + 1) * L["wslot_stride"]
-    assert L["region_stride"] >= (d.N + 1) * (L["wslot_stride"] + L["kvslot_stride"])
+    # attention slots (memory-saving variant) after the KV slots, sized for the
+    # full EP copy: Wqkv of Hq + 2 Hkv heads, then W_o (H x Hq*Dh)
+    assert L["attnslots_off"] == (d.N + 1) * (L["wslot_stride"] + L["kvslot_stride"])
+    if d.Hq:
+        assert L["attn_wo_off"] >= (d.Hq + 2 * d.Hkv) * d.D * d.H * 2 and L["attn_wo_off"] % 256 == 0
+        assert L["attnslot_stride"] >= L["attn_wo_off"] + d.H * d.Hq * d.D * 2
+        assert L["attnslot_stride"] % 4096 == 0
+    assert L["region_stride"] >= (d.N + 1) * (L["wslot_stride"] + L["kvslot_stride"] + L["attnslot_stride"])
     assert L["region_stride"] % (2 << 20) == 0
     assert L["ws_off"] == d.P * L["region_stride"]
 
@@ -166,9 +173,12 @@ def test_weights_exactly_once_tagged():
     del El
 
 
-def test_weights_round_trip_identity_and_untouched_bytes():
+@pytest.mark.parametrize("split", [0, 1])
+def test_weights_round_trip_identity_and_untouched_bytes(split):
+    """EP -> TP -> EP is the identity on every EP slot, for both W13 row
+    splits (R-2), and bytes that are not a destination keep their contents."""
     w = SMALL_W.with_(w_sigma=None)
-    d = dims_of(w)
+    d = dims_of(w, w13_split=split)
     L = oracle.layout(d)
     buf = fill_regions(L, w, seed=7)
     orig = buf.copy()
@@ -356,8 +366,10 @@ def test_kv_exactly_once_and_replication_tagged():
 def test_kv_round_trip_is_logically_identity():
     """EP -> TP -> EP with the greedy placement and fresh pages: every live
     (request, token, half, head, dim) value is back, now under its new owner's
-    pages (§3.2: no request dropped, same position)."""
-    for w in (TINY, SMALL_KV.with_(kv_sigma=None)):
+    pages (§3.2: no request dropped, same position).  Head sharing (Hkv < P),
+    one head per rank, and two heads per TP rank (Hkv = 2P: the TP page holds
+    a rank's heads side by side)."""
+    for w in (TINY, SMALL_KV.with_(kv_sigma=None), SMALL_KV.with_(Hkv=8, D=4, kv_sigma=None)):
         d, L, st, buf = _kv_setup(w)
         orig = buf.copy()
         assert oracle.kv_ep2tp(buf, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
@@ -478,6 +490,45 @@ def test_kv_validation_flags():
     many = np.zeros_like(st.owner)
     fl = oracle.kv_validate(d, 1, st.lens, many, st.ep_pt, st.tp_pt)
     assert fl & oracle.F_CAPACITY or fl & oracle.F_DUP_PAGE
+
+
+def test_kv_validation_boundaries():
+    """The bounds of the §4.5 capacity check and of the §3.2 page ids, worked
+    by hand: P = 2 ranks, Hkv = 2 (one head per TP rank), page size 4, a TP
+    pool of 8 pages (so 8 * h_tp / Hkv = 4 EP pages per rank) and room for 8
+    descriptors.  Lengths 9, 4, 7, 3, 2 take 3 + 1 + 2 + 1 + 1 = 8 pages; EP
+    owners 0, 1, 1, 0, 1 give rank 0 pages 3 + 1 = 4 and rank 1 1 + 2 + 1 = 4:
+    every pool exactly full, which both directions accept.  One token more on
+    the last request (5 tokens, 2 pages) overflows the TP pool, the
+    descriptor room and rank 1's EP pool; a page id equal to its pool size is
+    out of range."""
+    d = oracle.Dims(P=2, N=1, Hkv=2, D=4, ps=4, pages_tp=8, max_requests=5, max_pages=8)
+    assert oracle.layout(d)["pages_ep"] == 4
+    lens = np.array([9, 4, 7, 3, 2], np.int32)
+    owner = np.array([0, 1, 1, 0, 1], np.int32)
+    ep_pt = np.full((5, 3), -1, np.int32)
+    tp_pt = np.full((5, 3), -1, np.int32)
+    ep_pt[0, :3], ep_pt[3, 0] = [0, 1, 2], 3             # rank 0: EP pages 0..3
+    ep_pt[1, 0], ep_pt[2, :2], ep_pt[4, 0] = 0, [1, 2], 3  # rank 1: EP pages 0..3
+    tp_pt[0, :3], tp_pt[1, 0], tp_pt[2, :2], tp_pt[3, 0], tp_pt[4, 0] = [0, 1, 2], 3, [4, 5], 6, 7
+    for direction in (0, 1):
+        assert oracle.kv_validate(d, direction, lens, owner, ep_pt, tp_pt) == 0
+        longer = lens.copy()
+        longer[4] = 5
+        ep2, tp2 = ep_pt.copy(), tp_pt.copy()
+        ep2[4, 1], tp2[4, 1] = 0, 0                      # ids of the extra page (never reached)
+        assert oracle.kv_validate(d, direction, longer, owner, ep2, tp2) == oracle.F_CAPACITY
+        bad = tp_pt.copy()
+        bad[3, 0] = 8                                     # = pages_tp
+        assert oracle.kv_validate(d, direction, lens, owner, ep_pt, bad) == oracle.F_PAGE_OOB
+        bad = ep_pt.copy()
+        bad[3, 0] = 4                                     # = pages_ep
+        assert oracle.kv_validate(d, direction, lens, owner, bad, tp_pt) == oracle.F_PAGE_OOB
+    # TP -> EP only: rank 1 one page over its pool while the totals still fit
+    owner2 = owner.copy()
+    owner2[3] = 1                                         # rank 1: 4 + 1 = 5 > 4
+    assert oracle.kv_validate(d, 1, lens, owner2, ep_pt, tp_pt) == oracle.F_CAPACITY
+    assert oracle.kv_validate(d, 0, lens, owner2, ep_pt, tp_pt) == 0
 
 
 def test_kv_descriptors_cover_every_live_token():

@@ -23,20 +23,26 @@ def run_lib(umm, t_high, t_low, window, cooldown, start_mode, counts, times, fit
     return out, state
 
 
-def test_policy_golden_trace(umm):
-    lines = read_golden("policy_trace.txt")
+@pytest.mark.parametrize("name", ["policy_trace.txt", "policy_boundaries.txt"])
+def test_policy_golden_trace(umm, name):
+    """Hand-worked traces: the §6.1 settings over a burst, and the edges of
+    each rule (thresholds met exactly, a window not yet full, the last step
+    of a cooldown)."""
+    lines = read_golden(name)
     p = lines[0].split(":")[1].split()
     t_high, t_low, window, cool = float(p[0]), float(p[1]), int(p[2]), float(p[3])
     start = umm.UMM_MODE_TP if p[4] == "TP" else umm.UMM_MODE_EP
-    rows = [ints(ln) for ln in lines[1:]]
+    f = lines[1].split(":")[1].split()
+    final = (umm.UMM_MODE_TP if f[0] == "TP" else umm.UMM_MODE_EP, int(f[1]), int(f[2]))
+    rows = [ints(ln) for ln in lines[2:]]
     times = [r[0] for r in rows]
     counts = [r[1] for r in rows]
     fits = [bool(r[2]) for r in rows]
     want = [r[3] for r in rows]
-    got, (mode, switches, cancels) = run_lib(umm, t_high, t_low, window, cool, start, counts, times, fits)
+    got, state = run_lib(umm, t_high, t_low, window, cool, start, counts, times, fits)
     assert got == want
-    assert (mode, switches, cancels) == (umm.UMM_MODE_TP, 4, 1)
-    assert ref.run(t_high, t_low, window, cool, ref.TP, counts, times, fits) == want
+    assert state == final
+    assert ref.run(t_high, t_low, window, cool, ref.TP if p[4] == "TP" else ref.EP, counts, times, fits) == want
 
 
 def bursty(seed, n):
