@@ -237,15 +237,22 @@ def umm_layout_for_dims(dims: UmmDims) -> dict:
     return out.as_dict()
 
 
+# ranks (P) of the handles made through this module: the size checks of the
+# per-rank free lists need it
+_RANKS: dict[int, int] = {}
+
+
 def umm_create(dims: UmmDims, d_base, nbytes: int) -> int:
     h = ctypes.c_void_p()
     base = _buf(d_base, int(nbytes), "umm_create", "d_base")
     _ck(_lib.umm_create(ctypes.byref(dims), base, int(nbytes), ctypes.byref(h)), "umm_create")
+    _RANKS[h.value] = int(dims.P)
     return h.value
 
 
 def umm_destroy(h: int) -> None:
     _ck(_lib.umm_destroy(h), "umm_destroy")
+    _RANKS.pop(h, None)
 
 
 def umm_layout(h: int) -> dict:
@@ -395,12 +402,13 @@ def umm_switch_ep2tp(h: int, R: int, max_pages_per_req: int, seq_lens, ep_owner,
 def umm_switch_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, tp_pos, tp_page_table, ep_free_pages,
                      ep_free_stride: int, ep_free_count: int, ep_owner, local_pos, ep_page_table,
                      stream=None) -> None:
-    # the number of pools (P) is not known here: the free lists are checked
-    # for one pool's count; the library reads (P-1) * stride + count entries
+    # the library reads (P-1) * stride + count free-list entries; P is known
+    # for handles made through this module (else one pool's count is checked)
     w, n, t = "umm_switch_tp2ep", max(R, 0), max(R, 0) * max(max_pages_per_req, 0)
+    nfree = (_RANKS.get(h, 1) - 1) * max(int(ep_free_stride), 0) + max(int(ep_free_count), 0)
     _ck(_lib.umm_switch_tp2ep(h, R, max_pages_per_req, _arr(seq_lens, n, w, "seq_lens"),
                               _arr(tp_pos, n, w, "tp_pos"), _arr(tp_page_table, t, w, "tp_page_table"),
-                              _arr(ep_free_pages, max(int(ep_free_count), 0), w, "ep_free_pages"),
+                              _arr(ep_free_pages, nfree, w, "ep_free_pages"),
                               int(ep_free_stride), int(ep_free_count), _arr(ep_owner, n, w, "ep_owner"),
                               _arr(local_pos, n, w, "local_pos"), _arr(ep_page_table, t, w, "ep_page_table"),
                               _stream(stream)), w)

@@ -262,9 +262,16 @@ def test_binding_refuses_arrays_that_cannot_be_the_kernels_input(umm, monkeypatc
         umm.umm_assign_pages(0x1, 3, R, ok_vec, ok_vec, ok_vec, _FakeTensor(2 * 8 + 4), 8, 5, ok_tab, maxp)
     assert ei.value.code == umm.UMM_ERR_INVALID_ARG
     umm.umm_assign_pages(0x1, 3, R, ok_vec, ok_vec, ok_vec, _FakeTensor(2 * 8 + 5), 8, 5, ok_tab, maxp)
+    umm._RANKS[0x5] = 4                                                  # a handle of 4 ranks
+    with pytest.raises(umm.UmmError) as ei:                              # 4 pools need 3*stride + count
+        umm.umm_switch_tp2ep(0x5, R, maxp, ok_vec, ok_vec, ok_tab, _FakeTensor(3 * 10 + 6), 10, 7, ok_vec, ok_vec,
+                             ok_tab)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    umm.umm_switch_tp2ep(0x5, R, maxp, ok_vec, ok_vec, ok_tab, _FakeTensor(3 * 10 + 7), 10, 7, ok_vec, ok_vec, ok_tab)
+    del umm._RANKS[0x5]
     with pytest.raises(umm.UmmError) as ei:                              # buffer smaller than claimed
         umm.umm_create(lib_dims(umm, TINY), _FakeTensor(1000, dtype="torch.uint8", itemsize=1), 1001)
     assert ei.value.code == umm.UMM_ERR_INVALID_ARG
     with pytest.raises(umm.UmmError):
         umm.umm_create(lib_dims(umm, TINY), torch.zeros(64, dtype=torch.uint8), 64)
-    assert spy.calls == ["reshard_kv_ep2tp"] * 3 + ["umm_assign_pages"]
+    assert spy.calls == ["reshard_kv_ep2tp"] * 3 + ["umm_assign_pages", "umm_switch_tp2ep"]
