@@ -128,15 +128,40 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.selector = None
+
+    def _uuid(self):
+        """The timed device's UUID as nvidia-smi names it ("GPU-..."): the
+        index alone names another GPU when CUDA_VISIBLE_DEVICES remaps them."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.index).uuid)
+        except Exception:
+            return None
+        return u if u.startswith("GPU-") else "GPU-" + u
+
+    def _start(self, selector: str) -> bool:
+        try:                                   # does nvidia-smi know this GPU?
+            ok = subprocess.run(["nvidia-smi", "-i", selector, "--query-gpu=index", "--format=csv,noheader"],
+                                capture_output=True, timeout=20).returncode == 0
+        except subprocess.SubprocessError:
+            ok = False
+        if not ok:
+            return False
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", "-i", selector, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+             "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+        self.selector = selector
+        return True
 
     def __enter__(self):
         try:
             fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
             os.close(fd)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            uuid = self._uuid()
+            if not (uuid and self._start(uuid)):
+                self._start(str(self.index))
         except OSError:
             self.proc = None
         return self
@@ -172,7 +197,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "gpu": self.selector}
 
 
 # ----------------------------------------------------------------------------- traffic from committed ncu summary
