@@ -279,11 +279,15 @@ def _check_kv_untouched(run: KVRun, rng):
         np.testing.assert_array_equal(_gather(dev, idx), _expect(dev, idx, True))
 
 
-@pytest.mark.parametrize("w", [KV_256REQ, FULL_SWITCH], ids=lambda w: w.name)
-def test_kv_and_full_switch_fullsize(w):
+@pytest.mark.parametrize("w,timed", [(KV_256REQ, False), (FULL_SWITCH, False), (FULL_SWITCH, True)],
+                         ids=["kv_256req", "full_switch", "full_switch_timed"])
+def test_kv_and_full_switch_fullsize(w, timed):
     """KV alone through the separate entry points; the full switch through
-    umm_switch_ep2tp / umm_switch_tp2ep, the calls bench.py times."""
+    umm_switch_ep2tp / umm_switch_tp2ep, the calls bench.py times: with the
+    layer copies chained, and with per-kernel timing on (timed: each launch
+    between two events, unchained), as in bench.py's timed steps."""
     dev = DevUMM(w, seed=w.seed)
+    umm.umm_profile_enable(dev.h, timed)
     run = KVRun(dev)
     rng = np.random.default_rng(1)
     switch = bool(w.E)
