@@ -487,8 +487,8 @@ def run_umm(args, rank, world, local_rank, w=None):
                 (sprof["weights_ep2tp"][1] + sprof["weights_tp2ep"][1]) /
                 (sprof["weights_ep2tp"][0] + sprof["weights_tp2ep"][0]), 4)
         if have_kv and sprof["kv_ep2tp"][0]:
-            staged["kv_ep2tp_ms_per_switch"] = round(sprof["kv_ep2tp"][1] / sprof["kv_ep2tp"][0], 3)
-            staged["kv_tp2ep_ms_per_switch"] = round(sprof["kv_tp2ep"][1] / sprof["kv_tp2ep"][0], 3)
+            staged["kv_ep2tp_ms_per_switch"] = round(sprof["kv_ep2tp"][1] / reps, 3)
+            staged["kv_tp2ep_ms_per_switch"] = round(sprof["kv_tp2ep"][1] / reps, 3)
         del stage_buf
         torch.cuda.empty_cache()
 

@@ -25,6 +25,7 @@ uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 struct Prof {
   int kind;
+  int units;   // layer copies (copy kinds) or calls (metadata kinds) timed
   cudaEvent_t a, b;
 };
 
@@ -176,10 +177,13 @@ unsigned int new_call(umm* u) {
 }
 
 // ---- per-kernel event timing ----
+// One event pair per scope.  The layer copies of one call sit in one scope
+// (units = their number), so the events never break their launch chain.
 struct ProfScope {
   umm* u;
   int kind;
   cudaStream_t s;
+  int units = 1;
   cudaEvent_t a = nullptr, b = nullptr;
   ProfScope(umm* uu, int k, cudaStream_t ss) : u(uu), kind(k), s(ss) {
     if (!u->prof || u->ev_pool.size() < 2) return;
@@ -192,16 +196,15 @@ struct ProfScope {
   ~ProfScope() {
     if (!a) return;
     cudaEventRecord(b, s);
-    u->pending.push_back(Prof{kind, a, b});
+    u->pending.push_back(Prof{kind, units, a, b});
   }
 };
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? UMM_OK : UMM_ERR_CUDA; }
 
 // Layer t of a call's copies runs as a programmatic dependent of layer t-1
-// (launch_chain).  Not while per-kernel timing is on: its events sit between
-// the launches, and each kernel is then timed on its own.
-bool chained(const umm* u, int t) { return t > 0 && !u->prof; }
+// (launch_chain); per-kernel timing brackets the whole chain (ProfScope).
+bool chained(int t) { return t > 0; }
 
 int check_kv_args(const umm* u, int32_t R, int32_t maxp, const void* a, const void* b, const void* c,
                   const void* d) {
@@ -233,12 +236,15 @@ int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, co
   if (rc) return rc;
   u->launches += R > 0 ? 2 : 1;
   const int N = u->dims.num_layers;
-  for (int t = 0; t < N; ++t) {
-    const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
+  {
     ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
-    rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(u, t)));
-    if (rc) return rc;
-    if (max_desc > 0) ++u->launches;
+    ps.units = max_desc > 0 ? N : 0;
+    for (int t = 0; t < N; ++t) {
+      const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
+      rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(t)));
+      if (rc) return rc;
+      if (max_desc > 0) ++u->launches;
+    }
   }
   u->kv_log.push_back(KvCall{call, u->kv_mode});
   if (u->kv_log.size() > 4096) u->kv_log.erase(u->kv_log.begin());
@@ -251,10 +257,11 @@ int reshard_weights(umm* u, int ep2tp, void* stream) {
   if (u->weight_mode != (ep2tp ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
   cudaStream_t s = as_stream(stream);
   const int N = u->dims.num_layers;
+  ProfScope ps(u, ep2tp ? UMM_K_WEIGHTS_EP2TP : UMM_K_WEIGHTS_TP2EP, s);
+  ps.units = N;
   for (int t = 0; t < N; ++t) {
     const int layer = ep2tp ? t : N - 1 - t;
-    ProfScope ps(u, ep2tp ? UMM_K_WEIGHTS_EP2TP : UMM_K_WEIGHTS_TP2EP, s);
-    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s, chained(u, t)));
+    int rc = cuda_rc(uk::launch_weights(u->geo, ep2tp, layer, s, chained(t)));
     if (rc) return rc;
     ++u->launches;
   }
@@ -281,6 +288,7 @@ int reshard_kv_staged(umm* u, int dir, void* d_stage, uint64_t stage_bytes, int3
   u->launches += R > 0 ? 2 : 1;
   {
     ProfScope ps(u, dir == 0 ? UMM_K_KV_EP2TP : UMM_K_KV_TP2EP, s);
+    ps.units = u->dims.num_layers;
     int n = 0;
     rc = cuda_rc(uk::launch_kv_staged(u->geo, u->ws, dir, R, lens, owner, static_cast<uint8_t*>(d_stage),
                                       reinterpret_cast<int64_t*>(u->geo.base + u->ws.order_tok),
@@ -450,10 +458,11 @@ static int reshard_attn(umm_t* u, int ep2tp, void* stream) {
   if (u->attn_mode != (ep2tp ? UMM_MODE_EP : UMM_MODE_TP)) return UMM_ERR_MODE;
   cudaStream_t s = as_stream(stream);
   const int N = u->dims.num_layers;
+  ProfScope ps(u, ep2tp ? UMM_K_ATTN_EP2TP : UMM_K_ATTN_TP2EP, s);
+  ps.units = N;
   for (int t = 0; t < N; ++t) {
     const int layer = ep2tp ? t : N - 1 - t;
-    ProfScope ps(u, ep2tp ? UMM_K_ATTN_EP2TP : UMM_K_ATTN_TP2EP, s);
-    int rc = cuda_rc(uk::launch_attn(u->geo, ep2tp, layer, s, chained(u, t)));
+    int rc = cuda_rc(uk::launch_attn(u->geo, ep2tp, layer, s, chained(t)));
     if (rc) return rc;
     ++u->launches;
   }
@@ -778,7 +787,7 @@ int umm_profile_read(umm_t* u, int32_t kind, int64_t* launches, double* total_ms
     float ms = 0.f;
     if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess)
       return UMM_ERR_CUDA;
-    u->prof_n[p.kind] += 1;
+    u->prof_n[p.kind] += p.units;
     u->prof_ms[p.kind] += ms;
     u->ev_pool.push_back(p.a);
     u->ev_pool.push_back(p.b);

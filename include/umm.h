@@ -47,8 +47,9 @@
  *  - The per-layer copies of one call (weights, KV, attention) are launched
  *    as a chain: layer k+1 uses programmatic dependent launch, so its CTAs
  *    may start, and read slots that no layer of the call writes, while layer
- *    k drains; each of its stores waits for layer k's grid to complete.  The
- *    chain is off while per-kernel timing (umm_profile_enable) is on.
+ *    k drains; each of its stores waits for layer k's grid to complete.
+ *    Per-kernel timing (umm_profile_enable) times the chain as a whole, so
+ *    it runs chained then too.
  *  - The library never aborts, traps or throws across this ABI.
  *  - A handle is not thread-safe: issue its calls from one host thread, with
  *    the buffer's device current.
@@ -383,7 +384,11 @@ int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags
 const char* umm_strerror(int code);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream
- * (diagnostics; not for use under graph capture).  Kinds: */
+ * (diagnostics; not for use under graph capture).  The layer copies of one
+ * call (weights, KV, attention; fused or staged) are timed by one event pair
+ * around all of them, so their launch chain stays intact, and count one unit
+ * per layer; the descriptor pass, placement, order and page hand-out count
+ * one unit per call.  Kinds: */
 #define UMM_K_WEIGHTS_EP2TP 0
 #define UMM_K_WEIGHTS_TP2EP 1
 #define UMM_K_KV_PREP       2
@@ -396,8 +401,9 @@ const char* umm_strerror(int code);
 #define UMM_K_ATTN_TP2EP    9
 #define UMM_K_COUNT         10
 int umm_profile_enable(umm_t* u, int32_t enable);
-/* Synchronises the recorded events; launches and summed milliseconds of one
- * kind since the last reset. */
+/* Synchronises the recorded events; units (see above) and summed
+ * milliseconds of one kind since the last reset: total_ms / units is the
+ * average time of one layer copy (or one call). */
 int umm_profile_read(umm_t* u, int32_t kind, int64_t* launches, double* total_ms);
 int umm_profile_reset(umm_t* u);
 

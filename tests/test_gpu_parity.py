@@ -480,9 +480,9 @@ def test_switch_entry_points_equal_oracle(w, mode):
     """umm_switch_ep2tp / umm_switch_tp2ep: weights, attention, request
     order, page hand-out and KV in one call each; the same bytes and metadata
     as the oracle's step-by-step definition, with the weights on the caller's
-    stream or on the handle's side stream (overlap).  Layer copies launch
-    chained (programmatic dependent launch) except under per-kernel timing
-    (timed), where each sits between two events: both give the same bytes."""
+    stream or on the handle's side stream (overlap), and with per-kernel
+    timing on (timed: one event pair around each call's chain of layer copies,
+    one unit counted per layer): the same bytes each way."""
     dev = DevUMM(w, seed=17)
     umm.umm_set_switch_overlap(dev.h, mode == "overlap")
     umm.umm_profile_enable(dev.h, mode == "timed")

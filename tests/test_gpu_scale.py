@@ -283,9 +283,9 @@ def _check_kv_untouched(run: KVRun, rng):
                          ids=["kv_256req", "full_switch", "full_switch_timed"])
 def test_kv_and_full_switch_fullsize(w, timed):
     """KV alone through the separate entry points; the full switch through
-    umm_switch_ep2tp / umm_switch_tp2ep, the calls bench.py times: with the
-    layer copies chained, and with per-kernel timing on (timed: each launch
-    between two events, unchained), as in bench.py's timed steps."""
+    umm_switch_ep2tp / umm_switch_tp2ep, the calls bench.py times, also with
+    per-kernel timing on (timed: events around each call's chain of layer
+    copies), as in bench.py's timed steps."""
     dev = DevUMM(w, seed=w.seed)
     umm.umm_profile_enable(dev.h, timed)
     run = KVRun(dev)
