@@ -501,11 +501,9 @@ def run_umm(args, rank, world, local_rank, w=None):
         h_ep_pt = pin(state["ep_pt"].cpu().numpy())
         h_tp_free = pin(tp_free.cpu().numpy())
         h_ep_free = pin(ep_free.cpu().numpy())
-        o_owner = torch.empty(R, dtype=torch.int32).pin_memory()
         o_local = torch.empty(R, dtype=torch.int32).pin_memory()
-        o_pt = torch.empty((R, maxp), dtype=torch.int32).pin_memory()
         h2d = sum(x.numel() * 4 for x in (h_lens, h_owner, h_ep_pt, h_tp_free, h_ep_free))
-        d2h = sum(x.numel() * 4 for x in (o_owner, o_local, o_pt)) + 8   # + status word read
+        d2h = sum(x.numel() * 4 for x in (h_owner, o_local, h_ep_pt)) + 8   # + status word read
         barrier()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
@@ -518,14 +516,14 @@ def run_umm(args, rank, world, local_rank, w=None):
                 ep_free.copy_(h_ep_free, non_blocking=True)
             step()
             with torch.cuda.stream(s):
-                o_owner.copy_(state["owner"], non_blocking=True)   # the new EP owners ...
+                # the new EP owners and their pages come back into the host
+                # arrays the next step sends (its EP state); local positions too
+                h_owner.copy_(state["owner"], non_blocking=True)
                 o_local.copy_(local, non_blocking=True)
-                o_pt.copy_(state["ep_pt"], non_blocking=True)      # ... and their pages
+                h_ep_pt.copy_(state["ep_pt"], non_blocking=True)
             code, _ = umm.umm_status_sync(h, s)                   # syncs the stream, reads status
             if code:
                 raise RuntimeError(f"e2e step failed: {umm.strerror(code)}")
-            h_owner.copy_(o_owner)                                 # next step starts from them
-            h_ep_pt.copy_(o_pt)
         wall = time.perf_counter() - wall0
         e2e_gbs = world * bytes_model["step"] * args.steps / wall / 1e9
         e2e = {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
