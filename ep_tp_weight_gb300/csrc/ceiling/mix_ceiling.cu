@@ -94,8 +94,10 @@ struct Case {
   } while (0)
 
 int main(int argc, char** argv) {
-  // GiB per buffer (1..16, default 8): nine buffers are allocated
+  // argv[1]: GiB per buffer (1..16, default 8); argv[2] (optional): run only
+  // case k of the list below (0..5), allocating only the buffers it uses
   const int gib = argc > 1 ? std::max(1, std::min(16, std::atoi(argv[1]))) : 8;
+  const int only = argc > 2 ? std::atoi(argv[2]) : -1;
   const size_t S = (size_t)gib << 30;
   const uint32_t n = (uint32_t)(S / kChunk);
   u256* src = nullptr;
@@ -103,7 +105,8 @@ int main(int argc, char** argv) {
   uint32_t *rperm = nullptr, *wperm = nullptr;
   CK(cudaMalloc(&src, S));
   CK(cudaMemset(src, 0x5a, S));
-  for (int k = 0; k < kMaxDst; ++k) {
+  const int ndst = only == 0 || only == 1 || only == 2 ? 1 : only == 3 || only == 4 ? 2 : kMaxDst;
+  for (int k = 0; k < ndst; ++k) {
     CK(cudaMalloc(&dst.d[k], S));
     CK(cudaMemset(dst.d[k], 0, S));
   }
@@ -128,7 +131,9 @@ int main(int argc, char** argv) {
       {"1R8W sequential", "attn_kernel TP->EP", 8, false, false},
   };
   const int reps = 10;
-  for (const Case& c : cases) {
+  for (int ci = 0; ci < (int)(sizeof(cases) / sizeof(cases[0])); ++ci) {
+    if (only >= 0 && ci != only) continue;
+    const Case& c = cases[ci];
     const uint32_t* rp = c.shuffled_reads ? rperm : nullptr;
     const uint32_t* wp = c.shuffled_writes ? wperm : nullptr;
     for (int w = 0; w < 3; ++w) mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
@@ -145,7 +150,7 @@ int main(int argc, char** argv) {
                 "\"ms_per_launch\": %.4f, \"GB_s\": %.1f}\n",
                 c.name, c.kernels, S, S * (size_t)c.nd, per, bytes / (per * 1e-3) / 1e9);
   }
-  for (int k = 0; k < kMaxDst; ++k) CK(cudaFree(dst.d[k]));
+  for (int k = 0; k < ndst; ++k) CK(cudaFree(dst.d[k]));
   CK(cudaFree(src));
   CK(cudaFree(rperm));
   CK(cudaFree(wperm));
