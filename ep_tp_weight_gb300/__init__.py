@@ -40,6 +40,7 @@ FLAG_CAPACITY = 2
 FLAG_PAGE_OOB = 4
 FLAG_DUP_PAGE = 8
 FLAG_ACCESS = 16
+FLAG_TIMEOUT = 32
 
 (K_WEIGHTS_EP2TP, K_WEIGHTS_TP2EP, K_KV_PREP, K_KV_EP2TP, K_KV_TP2EP, K_PLACE, K_ORDER, K_ASSIGN,
  K_ATTN_EP2TP, K_ATTN_TP2EP) = range(10)

@@ -729,8 +729,9 @@ int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags
   if (f & UMM_FLAG_PAGE_OOB) code = UMM_ERR_PAGE_OOB;
   if (f & UMM_FLAG_CAPACITY) code = UMM_ERR_CAPACITY;
   if (f & UMM_FLAG_BAD_REQUEST) code = UMM_ERR_BAD_REQUEST;
-  if (f & UMM_FLAG_ACCESS) code = UMM_ERR_ACCESS;   // checked build: a library fault
-  if (f & ~UMM_FLAG_ACCESS) {
+  if (f & UMM_FLAG_TIMEOUT) code = UMM_ERR_TIMEOUT;  // a bounded wait of a TMA copy gave up
+  if (f & UMM_FLAG_ACCESS) code = UMM_ERR_ACCESS;    // checked build: a library fault
+  if (f & ~(UMM_FLAG_ACCESS | UMM_FLAG_TIMEOUT)) {
     // the first KV reshard at or after the failing call did not run, nor did
     // any later one: the cache is still in the layout that call started from
     for (const KvCall& c : u->kv_log)

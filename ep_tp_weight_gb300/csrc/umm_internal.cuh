@@ -164,6 +164,22 @@ __device__ __forceinline__ bool access_ok(const Span& s, const void* a) {
   return true;
 }
 
+// The same test for an n-byte bulk (TMA) copy starting at a (16-byte aligned).
+__device__ __forceinline__ bool range_ok(const Span& s, const void* a, uint64_t n) {
+#ifdef UMM_CHECKED
+  const uint8_t* b = static_cast<const uint8_t*>(a);
+  if (b < s.lo || b + n > s.hi || (reinterpret_cast<uintptr_t>(b) & 15u) || (n & 15u)) {
+    atomicOr(s.flags, UMM_FLAG_ACCESS);
+    return false;
+  }
+#else
+  (void)s;
+  (void)a;
+  (void)n;
+#endif
+  return true;
+}
+
 // Everything a kernel needs to address the unified buffer.
 struct Geo {
   uint8_t* base;

@@ -9,10 +9,14 @@
 // per element).
 //
 // One launch per layer (kv_copy_*: one CTA per TP page, or per descriptor when
-// the pool is sparsely used; layers after the first chained, griddep_wait),
+// the pool is sparsely used; layers after the first chained, griddep_wait;
+// EP -> TP through TMA when every TP rank holds one head, kv_copy_ep2tp_tma),
 // driven by the descriptors of the descriptor pass
 // (umm_kv_prep.cu).  Nothing is written to the cache unless that pass raised
 // no flag.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "umm_scan.cuh"
 
 namespace uk {
@@ -170,6 +174,188 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
   griddep_wait();
 }
 
+// ------------------------------------------------------------------ EP -> TP through TMA
+
+// When every TP rank holds one head (Hkv <= P), a TP page of one head is
+// [ps rows][D] contiguous, while the same head is a strided column of the EP
+// page [ps][Hkv][D].  The TMA engine de-interleaves it: one tensor-map load
+// per (half, head) brings the head's ps rows of the EP page into a dense
+// shared-memory tile, and one bulk store per replica writes the tile's live
+// rows to the TP page.  One CTA (one thread issuing) per TP page; with
+// Hkv = 4, ps = 16, D = 128 a CTA holds 32 KiB of tiles and 7 fit an SM.
+// Measured on GB300 against kv_copy_ep2tp
+// with 32-byte vectors: 6.145 vs 6.164 ms per layer (full-switch workload),
+// 3.971 vs 3.989 ms (256 requests of 1k-32k tokens).
+struct TmaKVParams {
+  uint8_t* base;
+  const umm_kv_desc* desc;
+  const DevStatus* st;
+  unsigned int* flags;
+  const unsigned long long* sched;
+  unsigned int call;
+  uint64_t region_stride, kv_v_off, tp_slot;
+  uint32_t ps, Hkv, rep, tile_bytes, row_bytes;
+  uint32_t tile_stride;   // tile_bytes rounded up to 128 (TMA destination alignment)
+  long long pages_tp;
+  Span span;
+};
+
+constexpr uint32_t kTmaWaitTries = 1u << 22;   // bound of each mbarrier wait
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Waits, at most `tries` polls, for the phase `parity` of the mbarrier at
+// `bar` to complete; false if it did not.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t tries) {
+  for (uint32_t i = 0; i < tries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ CUtensorMap ep_map,
+                                                        const TmaKVParams p) {
+  extern __shared__ __align__(1024) uint8_t tiles[];   // [2 halves][Hkv heads][tile_stride]
+  __shared__ __align__(8) unsigned long long bar;
+  griddep_launch_dependents();
+  if (threadIdx.x != 0) return;
+  if (read_flags(p.st)) {
+    griddep_wait();
+    return;
+  }
+  const unsigned long long nd = p.sched ? (unsigned long long)p.pages_tp : p.st->ndesc;
+  const uint32_t b = smem_addr(&bar);
+  const uint32_t t0 = (smem_addr(tiles) + 127u) & ~127u;   // TMA destinations: 128-byte aligned
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  uint32_t parity = 0;
+  for (unsigned long long di = blockIdx.x; di < nd; di += gridDim.x) {
+    umm_kv_desc d;
+    if (p.sched) {
+      const unsigned long long e = p.sched[di];
+      const unsigned long long idx = e & 0xffffffffull;
+      if ((unsigned int)(e >> 32) != p.call || idx >= p.st->ndesc) continue;
+      d = p.desc[idx];
+    } else {
+      d = p.desc[di];
+    }
+    // loads: tensor coordinates (dim 0 first) {element, head, EP row, half, region}
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(2u * p.Hkv * p.tile_bytes)
+                 : "memory");
+    const int row0 = d.src_page * (int)p.ps;
+    for (uint32_t c = 0; c < 2; ++c)
+      for (uint32_t h = 0; h < p.Hkv; ++h)
+        asm volatile(
+            "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(t0 + (c * p.Hkv + h) * p.tile_stride),
+            "l"(&ep_map), "r"(0), "r"((int)h), "r"(row0), "r"((int)c), "r"(d.src_region), "r"(b)
+            : "memory");
+    if (!mbar_wait(b, parity, kTmaWaitTries)) {   // never expected: flag it, bound one more wait, leave
+      atomicOr(p.flags, UMM_FLAG_TIMEOUT);
+      mbar_wait(b, parity, kTmaWaitTries);
+      griddep_wait();
+      return;
+    }
+    parity ^= 1u;
+    griddep_wait();
+    // stores: the live rows of each head's tile to every TP rank holding it
+    const uint32_t nbytes = (uint32_t)d.ntok * p.row_bytes;
+    for (uint32_t c = 0; c < 2; ++c)
+      for (uint32_t h = 0; h < p.Hkv; ++h)
+        for (uint32_t j = 0; j < p.rep; ++j) {
+          uint8_t* const g = p.base + (uint64_t)(h * p.rep + j) * p.region_stride + p.tp_slot + c * p.kv_v_off +
+                             (uint64_t)d.dst_page * p.tile_bytes;
+          if (range_ok(p.span, g, nbytes))
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g),
+                         "r"(t0 + (c * p.Hkv + h) * p.tile_stride), "r"(nbytes)
+                         : "memory");
+        }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // tiles free for the next page
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  griddep_wait();
+}
+
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link to
+// libcuda); null if the driver does not offer it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    looked = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// Launches the TMA copy for one layer when the shape allows it; *done = false
+// (nothing enqueued) otherwise, and the caller uses kv_copy_ep2tp.
+cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t max_desc, cudaStream_t s,
+                             bool chained, bool* done) {
+  *done = false;
+  const uint64_t tile = (uint64_t)g.ps * (uint64_t)g.D * 2;
+  const uint64_t stride = (tile + 127) / 128 * 128;
+  const uint64_t smem = 2 * (uint64_t)g.Hkv * stride;
+  if (g.Hkv > g.P || g.D > 256 || g.ps > 256 || (g.D * 2) % 16 != 0 || smem + 128 > 48 * 1024 || max_desc <= 0)
+    return cudaSuccess;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaSuccess;
+  // the EP view of layer `layer` in every region: [region][half][row][head][element]
+  CUtensorMap map;
+  const cuuint64_t dims[5] = {(cuuint64_t)g.D, (cuuint64_t)g.Hkv, (cuuint64_t)g.pages_ep * (cuuint64_t)g.ps, 2,
+                              (cuuint64_t)g.P};
+  const cuuint64_t strides[4] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.Hkv * g.D * 2, (cuuint64_t)g.kv_v_off,
+                                 (cuuint64_t)g.region_stride};
+  const cuuint32_t box[5] = {(cuuint32_t)g.D, 1, (cuuint32_t)g.ps, 1, 1};
+  const cuuint32_t unit[5] = {1, 1, 1, 1, 1};
+  void* ep_slot = g.base + g.kvslots_off + (uint64_t)(layer + 1) * g.kvslot_stride;
+  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, ep_slot, dims, strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaSuccess;
+  TmaKVParams t;
+  t.base = g.base;
+  t.desc = p.desc;
+  t.st = p.st;
+  t.flags = g.flags;
+  t.sched = p.sched;
+  t.call = p.call;
+  t.region_stride = g.region_stride;
+  t.kv_v_off = g.kv_v_off;
+  t.tp_slot = p.tp_slot;
+  t.ps = (uint32_t)g.ps;
+  t.Hkv = (uint32_t)g.Hkv;
+  t.rep = p.rep;
+  t.tile_bytes = (uint32_t)tile;
+  t.tile_stride = (uint32_t)stride;
+  t.row_bytes = (uint32_t)g.D * 2;
+  t.pages_tp = g.pages_tp;
+  t.span = g.regions();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(max_desc < 0x7fffffffll ? max_desc : 0x7fffffffll));
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = (size_t)smem + 128;   // room to align the tiles
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  *done = true;
+  return cudaLaunchKernelEx(&cfg, kv_copy_ep2tp_tma, map, t);
+}
+
 namespace {
 // Threads and vectors per thread of the copies; one round of a CTA loads
 // 16 KiB in every shape below.  Picked by
@@ -234,6 +420,11 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.tok = FastDiv((uint32_t)g.Hkv * Dv);
   p.dv = FastDiv(Dv);
   p.span = g.regions();
+  if (dir == 0) {
+    bool done = false;
+    const cudaError_t e = launch_ep2tp_tma(g, p, layer, max_desc, s, chained, &done);
+    if (done || e != cudaSuccess) return e;
+  }
   switch (VB) {
     case 32: return run_copy<32>(p, dir, max_desc, s, chained);
     case 16: return run_copy<16>(p, dir, max_desc, s, chained);

@@ -81,7 +81,8 @@ extern "C" {
 #define UMM_ERR_PAGE_OOB     5  /* a page id outside its pool                             */
 #define UMM_ERR_CUDA         6  /* a CUDA runtime call failed (a launch of a multi-kernel
                                    call: the kernels enqueued before it stay enqueued)    */
-#define UMM_ERR_TIMEOUT      7  /* reserved: a bounded device wait gave up                */
+#define UMM_ERR_TIMEOUT      7  /* a bounded device wait (the mbarrier of a TMA copy) gave
+                                   up: that layer copy is incomplete                      */
 #define UMM_ERR_DUP_PAGE     8  /* two live pages would be written to one destination page */
 #define UMM_ERR_BAD_REQUEST  9  /* length < 0 or > max_pages_per_req*page_size, owner or
                                    list position out of range                             */
@@ -159,6 +160,7 @@ typedef struct {
 #define UMM_FLAG_PAGE_OOB    4u
 #define UMM_FLAG_DUP_PAGE    8u
 #define UMM_FLAG_ACCESS     16u   /* checked build only, see UMM_ERR_ACCESS */
+#define UMM_FLAG_TIMEOUT    32u   /* see UMM_ERR_TIMEOUT */
 
 /* One page-indexed work descriptor (§4.3): the live tokens of logical page
  * `page` of request `req`.  Descriptors are grouped by the rank whose bytes
@@ -374,10 +376,11 @@ int umm_kv_check_capacity(const umm_t* u, int32_t target_kv_mode, int32_t R,
                           const int32_t* h_seq_lens, const int32_t* h_ep_owner);
 
 /* Synchronise `stream`, read the sticky device flags, clear them, and return
- * the highest-priority code among them (BAD_REQUEST > CAPACITY > PAGE_OOB >
- * DUP_PAGE; UMM_OK if none) in *status_out (flags in *flags_out, may be
- * NULL).  If a KV reshard was stopped, the handle's KV mode is set back to
- * the layout the data is actually in. */
+ * the highest-priority code among them (ACCESS > TIMEOUT > BAD_REQUEST >
+ * CAPACITY > PAGE_OOB > DUP_PAGE; UMM_OK if none) in *status_out (flags in
+ * *flags_out, may be NULL).  If a KV reshard was stopped by a validation
+ * flag, the handle's KV mode is set back to the layout the data is actually
+ * in; ACCESS and TIMEOUT leave it (that reshard ran, with a copy missing). */
 int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags_out);
 
 /* Static description of a status code. */

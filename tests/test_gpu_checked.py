@@ -59,16 +59,21 @@ def test_checked_weights_fullsize():
 
 
 def test_access_flag_reported_and_cleared():
-    """FLAG_ACCESS, written into the status block from the host, comes back as
-    UMM_ERR_ACCESS ahead of every other flag and is cleared by the read.  It
-    does not roll the KV mode back (the switch ran), while a validation flag
-    from the same call does (that switch never ran)."""
+    """FLAG_ACCESS and FLAG_TIMEOUT (a bounded wait of the TMA copy gave up),
+    written into the status block from the host, come back as UMM_ERR_ACCESS
+    and UMM_ERR_TIMEOUT ahead of the validation flags and are cleared by the
+    read.  They do not roll the KV mode back (the switch ran), while a
+    validation flag from the same call does (that switch never ran).  No
+    wait is made to time out on the device."""
     from gpu_helpers import i32
     from helpers import initial_kv_state
     st_off = None
     for flags, want_code, want_kv in ((umm.FLAG_ACCESS, umm.UMM_ERR_ACCESS, umm.UMM_MODE_TP),
                                       (umm.FLAG_ACCESS | umm.FLAG_CAPACITY, umm.UMM_ERR_ACCESS, umm.UMM_MODE_EP),
-                                      (umm.FLAG_CAPACITY, umm.UMM_ERR_CAPACITY, umm.UMM_MODE_EP)):
+                                      (umm.FLAG_CAPACITY, umm.UMM_ERR_CAPACITY, umm.UMM_MODE_EP),
+                                      (umm.FLAG_TIMEOUT, umm.UMM_ERR_TIMEOUT, umm.UMM_MODE_TP),
+                                      (umm.FLAG_TIMEOUT | umm.FLAG_CAPACITY, umm.UMM_ERR_TIMEOUT, umm.UMM_MODE_EP),
+                                      (umm.FLAG_ACCESS | umm.FLAG_TIMEOUT, umm.UMM_ERR_ACCESS, umm.UMM_MODE_TP)):
         dev = DevUMM(TINY, seed=2)
         st = initial_kv_state(TINY, dev.d, dev.L, seed=2)
         st_off = dev.L["status_off"]
