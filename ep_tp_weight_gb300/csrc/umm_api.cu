@@ -215,8 +215,13 @@ int check_kv_args(const umm* u, int32_t R, int32_t maxp, const void* a, const vo
   return UMM_OK;
 }
 
+// tma: the EP->TP copy may run through TMA (kv_copy_ep2tp_tma).  A one-call
+// switch that runs the weight copies beside the KV (side stream) passes
+// false: beside them the LSU copy measured faster on GB300 (16 requests:
+// 6.15 vs 6.32 ms per round trip; 2048 requests: equal), while alone TMA is
+// faster.
 int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, const int32_t* owner,
-               const int32_t* ep_pt, const int32_t* tp_pt, void* stream) {
+               const int32_t* ep_pt, const int32_t* tp_pt, void* stream, bool tma = true) {
   int rc = check_kv_args(u, R, maxp, lens, owner, ep_pt, tp_pt);
   if (rc) return rc;
   const int32_t from = dir == 0 ? UMM_MODE_EP : UMM_MODE_TP;
@@ -241,7 +246,7 @@ int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, co
     ps.units = max_desc > 0 ? N : 0;
     for (int t = 0; t < N; ++t) {
       const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
-      rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(t)));
+      rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(t), tma));
       if (rc) return rc;
       if (max_desc > 0) ++u->launches;
     }
@@ -651,7 +656,9 @@ int umm_switch_ep2tp(umm_t* u, int32_t R, int32_t maxp, const int32_t* d_seq_len
                                tp_free_count, d_tp_page_table, maxp, stream)))
       return rc;
   }
-  if ((rc = reshard_kv(u, 0, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream))) return rc;
+  if ((rc = reshard_kv(u, 0, R, maxp, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table, stream,
+                       !ss.forked)))
+    return rc;
   return ss.join();
 }
 

@@ -233,7 +233,7 @@ cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_
 // the grid walks the TP page pool (descriptors in TP-page order, empty pages
 // exit at once); otherwise it walks the descriptor list.
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
-                           unsigned int call, cudaStream_t s, bool chained);
+                           unsigned int call, cudaStream_t s, bool chained, bool allow_tma = true);
 
 // The staged comparison path for the KV cache (gather -> exchange -> scatter
 // per rank through `stage`; the descriptor pass must have run first).

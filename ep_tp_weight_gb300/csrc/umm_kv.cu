@@ -387,7 +387,7 @@ cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
-                           unsigned int call, cudaStream_t s, bool chained) {
+                           unsigned int call, cudaStream_t s, bool chained, bool allow_tma) {
   int VB = 2;
   if (g.D % 16 == 0) VB = 32;
   else if (g.D % 8 == 0) VB = 16;
@@ -420,7 +420,7 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.tok = FastDiv((uint32_t)g.Hkv * Dv);
   p.dv = FastDiv(Dv);
   p.span = g.regions();
-  if (dir == 0) {
+  if (dir == 0 && allow_tma) {
     bool done = false;
     const cudaError_t e = launch_ep2tp_tma(g, p, layer, max_desc, s, chained, &done);
     if (done || e != cudaSuccess) return e;
