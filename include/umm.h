@@ -301,8 +301,13 @@ int umm_assign_pages(umm_t* u, int32_t npools, int32_t R, const int32_t* d_seq_l
  * t % page_size.  One descriptor-building pass (validation first), then one
  * gather/scatter launch per layer; each source row is read once and stored to
  * every replica.  Bytes of pages past a request's length, and of unused
- * pages, are not written.  Errors: MODE, INVALID_ARG (sync); BAD_REQUEST,
- * CAPACITY, PAGE_OOB, DUP_PAGE (device, before any write). */
+ * pages, are not written.  When every TP rank holds one head (num_kv_heads
+ * <= P) and a head row is a multiple of 16 bytes, the copy runs through TMA:
+ * tensor-map loads de-interleave each head of an EP page into shared memory
+ * and bulk stores write its live rows to each replica.  Errors: MODE,
+ * INVALID_ARG (sync); BAD_REQUEST, CAPACITY, PAGE_OOB, DUP_PAGE (device,
+ * before any write); TIMEOUT (the TMA copy's bounded wait gave up; not
+ * expected). */
 int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
                      const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
                      const int32_t* d_tp_page_table, void* stream);
