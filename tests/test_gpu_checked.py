@@ -51,7 +51,7 @@ def test_checked_fuzz(seed):
 
 
 def test_checked_full_switch_fullsize():
-    scale.test_kv_and_full_switch_fullsize(FULL_SWITCH, False)
+    scale.test_kv_and_full_switch_fullsize(FULL_SWITCH, False, False)
 
 
 def test_checked_weights_fullsize():

@@ -279,15 +279,19 @@ def _check_kv_untouched(run: KVRun, rng):
         np.testing.assert_array_equal(_gather(dev, idx), _expect(dev, idx, True))
 
 
-@pytest.mark.parametrize("w,timed", [(KV_256REQ, False), (FULL_SWITCH, False), (FULL_SWITCH, True)],
-                         ids=["kv_256req", "full_switch", "full_switch_timed"])
-def test_kv_and_full_switch_fullsize(w, timed):
+@pytest.mark.parametrize("w,timed,overlap", [(KV_256REQ, False, False), (FULL_SWITCH, False, False),
+                                             (FULL_SWITCH, True, False), (FULL_SWITCH, False, True)],
+                         ids=["kv_256req", "full_switch", "full_switch_timed", "full_switch_overlap"])
+def test_kv_and_full_switch_fullsize(w, timed, overlap):
     """KV alone through the separate entry points; the full switch through
     umm_switch_ep2tp / umm_switch_tp2ep, the calls bench.py times, also with
     per-kernel timing on (timed: events around each call's chain of layer
-    copies), as in bench.py's timed steps."""
+    copies), as in bench.py's timed steps, and with the weight copies on the
+    side stream (overlap), where KV EP->TP runs on the LSU copy instead of
+    the TMA one."""
     dev = DevUMM(w, seed=w.seed)
     umm.umm_profile_enable(dev.h, timed)
+    umm.umm_set_switch_overlap(dev.h, overlap)
     run = KVRun(dev)
     rng = np.random.default_rng(1)
     switch = bool(w.E)
