@@ -181,11 +181,12 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
 // page [ps][Hkv][D].  The TMA engine de-interleaves it: one tensor-map load
 // per (half, head) brings the head's ps rows of the EP page into a dense
 // shared-memory tile, and one bulk store per replica writes the tile's live
-// rows to the TP page.  One CTA (one thread issuing) per TP page; with
-// Hkv = 4, ps = 16, D = 128 a CTA holds 32 KiB of tiles and 7 fit an SM.
-// Measured on GB300 against kv_copy_ep2tp
-// with 32-byte vectors: 6.145 vs 6.164 ms per layer (full-switch workload),
-// 3.971 vs 3.989 ms (256 requests of 1k-32k tokens).
+// rows to the TP page.  One CTA (one thread issuing) per TP page and half
+// (K or V); with Hkv = 4, ps = 16, D = 128 a CTA holds 16 KiB of tiles.
+// Measured on GB300 against kv_copy_ep2tp with 32-byte vectors: 6.145 vs
+// 6.164 ms per layer (full-switch workload), 3.971 vs 3.989 ms (256 requests
+// of 1k-32k tokens), with one CTA per page; one per page and half then
+// measured 6.141 vs 6.147 ms and 3.968 vs 3.972 ms.
 struct TmaKVParams {
   uint8_t* base;
   const umm_kv_desc* desc;
@@ -221,7 +222,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 
 __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ CUtensorMap ep_map,
                                                         const TmaKVParams p) {
-  extern __shared__ __align__(1024) uint8_t tiles[];   // [2 halves][Hkv heads][tile_stride]
+  extern __shared__ __align__(1024) uint8_t tiles[];   // [Hkv heads][tile_stride] of half c
   __shared__ __align__(8) unsigned long long bar;
   griddep_launch_dependents();
   if (threadIdx.x != 0) return;
@@ -235,7 +236,8 @@ __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ 
   asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   uint32_t parity = 0;
-  for (unsigned long long di = blockIdx.x; di < nd; di += gridDim.x) {
+  const uint32_t c = blockIdx.x & 1u;
+  for (unsigned long long di = blockIdx.x >> 1; di < nd; di += gridDim.x >> 1) {
     umm_kv_desc d;
     if (p.sched) {
       const unsigned long long e = p.sched[di];
@@ -246,14 +248,13 @@ __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ 
       d = p.desc[di];
     }
     // loads: tensor coordinates (dim 0 first) {element, head, EP row, half, region}
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(2u * p.Hkv * p.tile_bytes)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(p.Hkv * p.tile_bytes)
                  : "memory");
     const int row0 = d.src_page * (int)p.ps;
-    for (uint32_t c = 0; c < 2; ++c)
-      for (uint32_t h = 0; h < p.Hkv; ++h)
+    for (uint32_t h = 0; h < p.Hkv; ++h)
         asm volatile(
             "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(t0 + (c * p.Hkv + h) * p.tile_stride),
+            " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(t0 + h * p.tile_stride),
             "l"(&ep_map), "r"(0), "r"((int)h), "r"(row0), "r"((int)c), "r"(d.src_region), "r"(b)
             : "memory");
     if (!mbar_wait(b, parity, kTmaWaitTries)) {   // never expected: flag it, bound one more wait, leave
@@ -266,14 +267,13 @@ __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ 
     griddep_wait();
     // stores: the live rows of each head's tile to every TP rank holding it
     const uint32_t nbytes = (uint32_t)d.ntok * p.row_bytes;
-    for (uint32_t c = 0; c < 2; ++c)
-      for (uint32_t h = 0; h < p.Hkv; ++h)
+    for (uint32_t h = 0; h < p.Hkv; ++h)
         for (uint32_t j = 0; j < p.rep; ++j) {
           uint8_t* const g = p.base + (uint64_t)(h * p.rep + j) * p.region_stride + p.tp_slot + c * p.kv_v_off +
                              (uint64_t)d.dst_page * p.tile_bytes;
           if (range_ok(p.span, g, nbytes))
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g),
-                         "r"(t0 + (c * p.Hkv + h) * p.tile_stride), "r"(nbytes)
+                         "r"(t0 + h * p.tile_stride), "r"(nbytes)
                          : "memory");
         }
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -306,7 +306,7 @@ cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t
   *done = false;
   const uint64_t tile = (uint64_t)g.ps * (uint64_t)g.D * 2;
   const uint64_t stride = (tile + 127) / 128 * 128;
-  const uint64_t smem = 2 * (uint64_t)g.Hkv * stride;
+  const uint64_t smem = (uint64_t)g.Hkv * stride;
   if (g.Hkv > g.P || g.D > 256 || g.ps > 256 || (g.D * 2) % 16 != 0 || smem + 128 > 48 * 1024 || max_desc <= 0)
     return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -343,7 +343,7 @@ cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t
   t.pages_tp = g.pages_tp;
   t.span = g.regions();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(max_desc < 0x7fffffffll ? max_desc : 0x7fffffffll));
+  cfg.gridDim = dim3((unsigned)(2 * max_desc < 0x7fffffffll ? 2 * max_desc : 0x7ffffffell));
   cfg.blockDim = dim3(32);
   cfg.dynamicSmemBytes = (size_t)smem + 128;   // room to align the tiles
   cfg.stream = s;
