@@ -75,11 +75,55 @@ __global__ void __launch_bounds__(kT) mix_copy(const u256* src, Dsts dst, int nd
   }
 }
 
+// The 1R1W sequential case through TMA: one thread per CTA bulk-loads its
+// 16 KiB chunk into shared memory (mbarrier, bounded wait) and bulk-stores it.
+__global__ void __launch_bounds__(32) bulk_copy(const u256* src, u256* dst, uint32_t nchunks) {
+  extern __shared__ __align__(128) uint8_t buf[];
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x != 0 || blockIdx.x >= nchunks) return;
+  const uint32_t s0 = ((uint32_t)__cvta_generic_to_shared(buf) + 127u) & ~127u;
+  const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+  const u256* from = src + (size_t)blockIdx.x * kChunkVec;
+  u256* to = dst + (size_t)blockIdx.x * kChunkVec;
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"((uint32_t)kChunk) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(s0), "l"(from), "r"((uint32_t)kChunk), "r"(b)
+               : "memory");
+  for (uint32_t i = 0; i < (1u << 22); ++i) {   // bounded wait for the load
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done)
+                 : "r"(b)
+                 : "memory");
+    if (done) {
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(to), "r"(s0),
+                   "r"((uint32_t)kChunk)
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      return;
+    }
+  }
+  for (uint32_t i = 0; i < (1u << 22); ++i) {   // never expected: wait as long again for the load, then leave
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done)
+                 : "r"(b)
+                 : "memory");
+    if (done) return;
+  }
+}
+
 struct Case {
   const char* name;
   const char* kernels;   // reshard kernels with this pattern
   int nd;
   bool shuffled_reads, shuffled_writes;
+  bool tma = false;      // bulk_copy instead of mix_copy (1R1W sequential only)
 };
 
 }  // namespace
@@ -95,7 +139,7 @@ struct Case {
 
 int main(int argc, char** argv) {
   // argv[1]: GiB per buffer (1..16, default 8); argv[2] (optional): run only
-  // case k of the list below (0..5), allocating only the buffers it uses
+  // case k of the list below (0..6), allocating only the buffers it uses
   const int gib = argc > 1 ? std::max(1, std::min(16, std::atoi(argv[1]))) : 8;
   const int only = argc > 2 ? std::atoi(argv[2]) : -1;
   const size_t S = (size_t)gib << 30;
@@ -105,7 +149,7 @@ int main(int argc, char** argv) {
   uint32_t *rperm = nullptr, *wperm = nullptr;
   CK(cudaMalloc(&src, S));
   CK(cudaMemset(src, 0x5a, S));
-  const int ndst = only == 0 || only == 1 || only == 2 ? 1 : only == 3 || only == 4 ? 2 : kMaxDst;
+  const int ndst = only == 0 || only == 1 || only == 2 || only == 6 ? 1 : only == 3 || only == 4 ? 2 : kMaxDst;
   for (int k = 0; k < ndst; ++k) {
     CK(cudaMalloc(&dst.d[k], S));
     CK(cudaMemset(dst.d[k], 0, S));
@@ -129,6 +173,7 @@ int main(int argc, char** argv) {
       {"1R2W sequential", "", 2, false, false},
       {"1R2W shuffled reads", "kv_copy_ep2tp", 2, true, false},
       {"1R8W sequential", "attn_kernel TP->EP", 8, false, false},
+      {"1R1W sequential, TMA bulk copies", "", 1, false, false, true},
   };
   const int reps = 10;
   for (int ci = 0; ci < (int)(sizeof(cases) / sizeof(cases[0])); ++ci) {
@@ -136,11 +181,15 @@ int main(int argc, char** argv) {
     const Case& c = cases[ci];
     const uint32_t* rp = c.shuffled_reads ? rperm : nullptr;
     const uint32_t* wp = c.shuffled_writes ? wperm : nullptr;
-    for (int w = 0; w < 3; ++w) mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
+    auto launch = [&]() {
+      if (c.tma) bulk_copy<<<n, 32, kChunk + 128>>>(src, dst.d[0], n);
+      else mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
+    };
+    for (int w = 0; w < 3; ++w) launch();
     CK(cudaGetLastError());
     CK(cudaDeviceSynchronize());
     CK(cudaEventRecord(e0));
-    for (int r = 0; r < reps; ++r) mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
+    for (int r = 0; r < reps; ++r) launch();
     CK(cudaEventRecord(e1));
     CK(cudaEventSynchronize(e1));
     float ms = 0.f;
