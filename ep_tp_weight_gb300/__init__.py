@@ -35,6 +35,9 @@ UMM_ERR_ACCESS = 10
 UMM_MODE_EP = 0
 UMM_MODE_TP = 1
 
+UMM_KV_COPY_LSU = 0
+UMM_KV_COPY_TMA = 1
+
 FLAG_BAD_REQUEST = 1
 FLAG_CAPACITY = 2
 FLAG_PAGE_OOB = 4
@@ -124,6 +127,8 @@ _SIG = {
     "umm_switch_ep2tp": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
     "umm_switch_tp2ep": [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp],
     "umm_set_switch_overlap": [_vp, _i32],
+    "umm_kv_copy_kernel": [_P(UmmDims), _i32, _P(_i32), _P(_i32)],
+    "umm_test_stall_tma_wait": [_vp, _i32, ctypes.c_uint32],
     "umm_policy_create": [_vp, _P(_vp)],
     "umm_policy_destroy": [_vp],
     "umm_policy_step": [_vp, _i64, ctypes.c_double, _i32, _P(_i32)],
@@ -417,6 +422,21 @@ def umm_switch_tp2ep(h: int, R: int, max_pages_per_req: int, seq_lens, tp_pos, t
 
 def umm_set_switch_overlap(h: int, enable: bool = True) -> None:
     _ck(_lib.umm_set_switch_overlap(h, 1 if enable else 0), "umm_set_switch_overlap")
+
+
+def umm_kv_copy_kernel(dims: UmmDims, direction: int) -> tuple[int, int]:
+    """(UMM_KV_COPY_TMA or UMM_KV_COPY_LSU, LSU vector bytes or 0) that a KV
+    reshard of these dims launches (host-only)."""
+    k, vb = ctypes.c_int32(), ctypes.c_int32()
+    _ck(_lib.umm_kv_copy_kernel(ctypes.byref(dims), int(direction), ctypes.byref(k), ctypes.byref(vb)),
+        "umm_kv_copy_kernel")
+    return k.value, vb.value
+
+
+def umm_test_stall_tma_wait(h: int, layer: int, polls: int) -> None:
+    """Checked build only: make the TMA copy of one KV EP->TP layer run out a
+    wait (see include/umm.h)."""
+    _ck(_lib.umm_test_stall_tma_wait(h, int(layer), int(polls)), "umm_test_stall_tma_wait")
 
 
 def umm_kv_check_capacity(h: int, target_kv_mode: int, R: int, h_seq_lens, h_ep_owner=None) -> int:

@@ -57,6 +57,10 @@ struct umm {
   bool overlap = false;
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // umm_test_stall_tma_wait (checked build): the KV EP->TP layer whose TMA
+  // copy makes one wait that runs out after test_stall_polls polls
+  int32_t test_stall_layer = -1;
+  uint32_t test_stall_polls = 0;
 };
 
 namespace {
@@ -169,6 +173,37 @@ void compute_layout(const umm_dims* d, umm_layout_t* L, uk::Ws* ws) {
   L->desc_capacity = desc_cap;
 }
 
+// What the kernels need to address a buffer at `base` laid out as L.
+uk::Geo make_geo(const umm_dims* dims, const umm_layout_t& L, const uk::Ws& ws, uint8_t* base) {
+  uk::Geo g;
+  g.base = base;
+  g.region_stride = L.region_stride;
+  g.wslot_stride = L.wslot_stride;
+  g.w13_off = L.w13_off;
+  g.w2_off = L.w2_off;
+  g.kvslot_stride = L.kvslot_stride;
+  g.kv_v_off = L.kv_v_off;
+  g.kvslots_off = L.kvslots_off;
+  g.P = dims->P;
+  g.E = dims->E;
+  g.H = dims->H;
+  g.I = dims->I;
+  g.N = dims->num_layers;
+  g.Hkv = dims->num_kv_heads;
+  g.D = dims->head_dim;
+  g.ps = dims->page_size;
+  g.w13_split = dims->w13_split;
+  g.Hq = dims->attn_q_heads;
+  g.attnslot_stride = L.attnslot_stride;
+  g.attn_wo_off = L.attn_wo_off;
+  g.attnslots_off = L.attnslots_off;
+  g.flags = base ? reinterpret_cast<unsigned int*>(base + ws.status) : nullptr;
+  g.pages_ep = L.pages_ep;
+  g.pages_tp = L.pages_tp;
+  g.h_tp = L.h_tp;
+  return g;
+}
+
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 unsigned int new_call(umm* u) {
@@ -246,7 +281,9 @@ int reshard_kv(umm* u, int dir, int32_t R, int32_t maxp, const int32_t* lens, co
     ps.units = max_desc > 0 ? N : 0;
     for (int t = 0; t < N; ++t) {
       const int layer = dir == 0 ? t : N - 1 - t;   // EP->TP ascending, TP->EP descending
-      rc = cuda_rc(uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(t), tma));
+      const uint32_t stall = dir == 0 && layer == u->test_stall_layer ? u->test_stall_polls : 0u;
+      rc = cuda_rc(
+          uk::launch_kv_copy(u->geo, u->ws, dir, layer, max_desc, use_sched, call, s, chained(t), tma, stall));
       if (rc) return rc;
       if (max_desc > 0) ++u->launches;
     }
@@ -351,6 +388,20 @@ int umm_layout_for_dims(const umm_dims* dims, umm_layout_t* out) {
   return UMM_OK;
 }
 
+int umm_kv_copy_kernel(const umm_dims* dims, int32_t dir, int32_t* kernel, int32_t* vector_bytes) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (dims->num_kv_heads == 0 || (dir != 0 && dir != 1) || !kernel) return UMM_ERR_INVALID_ARG;
+  umm_layout_t L;
+  uk::Ws ws;
+  compute_layout(dims, &L, &ws);
+  const uk::Geo g = make_geo(dims, L, ws, nullptr);
+  const bool tma = dir == 0 && uk::ep2tp_tma_shape(g);
+  *kernel = tma ? UMM_KV_COPY_TMA : UMM_KV_COPY_LSU;
+  if (vector_bytes) *vector_bytes = tma ? 0 : uk::kv_vector_bytes(g);
+  return UMM_OK;
+}
+
 int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) {
   int rc = check_dims(dims);
   if (rc) return rc;
@@ -380,32 +431,8 @@ int umm_create(const umm_dims* dims, void* d_base, uint64_t bytes, umm_t** out) 
   }
   cudaDeviceGetAttribute(&u->sms, cudaDevAttrMultiProcessorCount, u->device);
   if (u->sms < 1) u->sms = 1;
+  u->geo = make_geo(dims, u->L, u->ws, static_cast<uint8_t*>(d_base));
   uk::Geo& g = u->geo;
-  g.base = static_cast<uint8_t*>(d_base);
-  g.region_stride = u->L.region_stride;
-  g.wslot_stride = u->L.wslot_stride;
-  g.w13_off = u->L.w13_off;
-  g.w2_off = u->L.w2_off;
-  g.kvslot_stride = u->L.kvslot_stride;
-  g.kv_v_off = u->L.kv_v_off;
-  g.kvslots_off = u->L.kvslots_off;
-  g.P = dims->P;
-  g.E = dims->E;
-  g.H = dims->H;
-  g.I = dims->I;
-  g.N = dims->num_layers;
-  g.Hkv = dims->num_kv_heads;
-  g.D = dims->head_dim;
-  g.ps = dims->page_size;
-  g.w13_split = dims->w13_split;
-  g.Hq = dims->attn_q_heads;
-  g.attnslot_stride = u->L.attnslot_stride;
-  g.attn_wo_off = u->L.attn_wo_off;
-  g.attnslots_off = u->L.attnslots_off;
-  g.flags = reinterpret_cast<unsigned int*>(g.base + u->ws.status);
-  g.pages_ep = u->L.pages_ep;
-  g.pages_tp = u->L.pages_tp;
-  g.h_tp = u->L.h_tp;
   u->weight_mode = dims->weight_mode;
   u->kv_mode = dims->kv_mode;
   u->attn_mode = dims->attn_mode;
@@ -582,6 +609,20 @@ int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
                      const int32_t* d_tp_page_table, void* stream) {
   return reshard_kv(u, 1, R, max_pages_per_req, d_seq_lens, d_ep_owner, d_ep_page_table, d_tp_page_table,
                     stream);
+}
+
+int umm_test_stall_tma_wait(umm_t* u, int32_t layer, uint32_t polls) {
+#ifdef UMM_CHECKED
+  if (!u || layer < -1 || layer >= u->dims.num_layers) return UMM_ERR_INVALID_ARG;
+  u->test_stall_layer = polls ? layer : -1;
+  u->test_stall_polls = layer >= 0 ? polls : 0u;
+  return UMM_OK;
+#else
+  (void)u;
+  (void)layer;
+  (void)polls;
+  return UMM_ERR_INVALID_ARG;   // only the checked build carries the hook
+#endif
 }
 
 int umm_set_switch_overlap(umm_t* u, int32_t enable) {

@@ -231,9 +231,15 @@ cudaError_t launch_kv_prep(const Geo& g, const Ws& w, int dir, int32_t R, int32_
                            const int32_t* tp_pt, unsigned int call, int use_sched, cudaStream_t s, int sms);
 // max_desc: an upper bound on the descriptors of the call.  With use_sched
 // the grid walks the TP page pool (descriptors in TP-page order, empty pages
-// exit at once); otherwise it walks the descriptor list.
+// exit at once); otherwise it walks the descriptor list.  stall_polls (checked
+// build, tests only): the TMA copy's extra wait that runs out (0 = off).
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
-                           unsigned int call, cudaStream_t s, bool chained, bool allow_tma = true);
+                           unsigned int call, cudaStream_t s, bool chained, bool allow_tma = true,
+                           uint32_t stall_polls = 0);
+// Host-side choices of launch_kv_copy: whether KV EP->TP can run through the
+// TMA copy, and the vector width (bytes) of the LSU copies.
+bool ep2tp_tma_shape(const Geo& g);
+int kv_vector_bytes(const Geo& g);
 
 // The staged comparison path for the KV cache (gather -> exchange -> scatter
 // per rank through `stage`; the descriptor pass must have run first).

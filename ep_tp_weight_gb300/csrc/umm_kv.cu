@@ -187,6 +187,12 @@ __global__ void __launch_bounds__(T) kv_copy_tp2ep(const KVParams p) {
 // 6.164 ms per layer (full-switch workload), 3.971 vs 3.989 ms (256 requests
 // of 1k-32k tokens), with one CTA per page; one per page and half then
 // measured 6.141 vs 6.147 ms and 3.968 vs 3.972 ms.
+//
+// Tensor coordinates are signed 32-bit.  Each half (K, V) has its own map
+// whose dimensions are {element, head, row in page, page, region}, so a load
+// is addressed by the page id itself, never by page * page_size: every
+// coordinate stays below 2^31 for every pool size the handle accepts
+// (kv_pages_tp < 2^31, and pages_ep <= pages_tp).
 struct TmaKVParams {
   uint8_t* base;
   const umm_kv_desc* desc;
@@ -197,6 +203,7 @@ struct TmaKVParams {
   uint64_t region_stride, kv_v_off, tp_slot;
   uint32_t ps, Hkv, rep, tile_bytes, row_bytes;
   uint32_t tile_stride;   // tile_bytes rounded up to 128 (TMA destination alignment)
+  uint32_t stall_polls;   // checked build, tests only: see kv_copy_ep2tp_tma (0 = off)
   long long pages_tp;
   Span span;
 };
@@ -220,7 +227,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return false;
 }
 
-__global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ CUtensorMap ep_map,
+__global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ CUtensorMap map_k,
+                                                        const __grid_constant__ CUtensorMap map_v,
                                                         const TmaKVParams p) {
   extern __shared__ __align__(1024) uint8_t tiles[];   // [Hkv heads][tile_stride] of half c
   __shared__ __align__(8) unsigned long long bar;
@@ -237,6 +245,7 @@ __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ 
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   uint32_t parity = 0;
   const uint32_t c = blockIdx.x & 1u;
+  const CUtensorMap* const map = c ? &map_v : &map_k;
   for (unsigned long long di = blockIdx.x >> 1; di < nd; di += gridDim.x >> 1) {
     umm_kv_desc d;
     if (p.sched) {
@@ -247,17 +256,37 @@ __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ 
     } else {
       d = p.desc[di];
     }
-    // loads: tensor coordinates (dim 0 first) {element, head, EP row, half, region}
+    // loads: tensor coordinates (dim 0 first) {element, head, row in page, page, region}
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(p.Hkv * p.tile_bytes)
                  : "memory");
-    const int row0 = d.src_page * (int)p.ps;
     for (uint32_t h = 0; h < p.Hkv; ++h)
         asm volatile(
             "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
             " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(t0 + h * p.tile_stride),
-            "l"(&ep_map), "r"(0), "r"((int)h), "r"(row0), "r"((int)c), "r"(d.src_region), "r"(b)
+            "l"(map), "r"(0), "r"((int)h), "r"(0), "r"(d.src_page), "r"(d.src_region), "r"(b)
             : "memory");
-    if (!mbar_wait(b, parity, kTmaWaitTries)) {   // never expected: flag it, bound one more wait, leave
+    bool landed = mbar_wait(b, parity, kTmaWaitTries);
+#ifdef UMM_CHECKED
+    // test hook (checked build only): after the loads above have landed, one
+    // more wait, on a barrier that expects two arrivals and gets one, which
+    // therefore runs out after p.stall_polls polls and takes the timeout exit
+    // below with no copy in flight
+    if (landed && p.stall_polls) {
+      __shared__ __align__(8) unsigned long long never;
+      const uint32_t nb = smem_addr(&never);
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(nb) : "memory");
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(nb) : "memory");
+      landed = mbar_wait(nb, 0, p.stall_polls);
+    }
+#endif
+    if (!landed) {
+      // Never expected.  Flag it; wait, again at most kTmaWaitTries polls,
+      // for this CTA's loads; store nothing and leave.  Later kernels of the
+      // call see the flag and do nothing.  Should that wait run out as well,
+      // a load may still be writing this CTA's shared memory after it exits:
+      // the status (UMM_ERR_TIMEOUT) then tells the caller that this call's
+      // KV contents are undefined.
       atomicOr(p.flags, UMM_FLAG_TIMEOUT);
       mbar_wait(b, parity, kTmaWaitTries);
       griddep_wait();
@@ -299,31 +328,44 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Launches the TMA copy for one layer when the shape allows it; *done = false
-// (nothing enqueued) otherwise, and the caller uses kv_copy_ep2tp.
-cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t max_desc, cudaStream_t s,
-                             bool chained, bool* done) {
-  *done = false;
+// Whether the shape lets KV EP->TP run through kv_copy_ep2tp_tma: one head
+// per TP rank (Hkv <= P), a head row a multiple of 16 bytes (bulk-copy
+// sizes), boxes of at most 256 per dimension, the tiles within the default
+// 48 KiB of shared memory, and every tensor coordinate below 2^31.
+bool ep2tp_tma_shape(const Geo& g) {
   const uint64_t tile = (uint64_t)g.ps * (uint64_t)g.D * 2;
   const uint64_t stride = (tile + 127) / 128 * 128;
   const uint64_t smem = (uint64_t)g.Hkv * stride;
-  if (g.Hkv > g.P || g.D > 256 || g.ps > 256 || (g.D * 2) % 16 != 0 || smem + 128 > 48 * 1024 || max_desc <= 0)
-    return cudaSuccess;
+  return g.Hkv >= 1 && g.Hkv <= g.P && g.D <= 256 && g.ps <= 256 && (g.D * 2) % 16 == 0 && smem + 128 <= 48 * 1024 &&
+         g.pages_ep >= 1 && g.pages_ep <= 0x7fffffffll && g.P <= 0x7fffffff;
+}
+
+// Launches the TMA copy for one layer when the shape allows it; *done = false
+// (nothing enqueued) otherwise, and the caller uses kv_copy_ep2tp.
+cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t max_desc, cudaStream_t s,
+                             bool chained, uint32_t stall_polls, bool* done) {
+  *done = false;
+  if (!ep2tp_tma_shape(g) || max_desc <= 0) return cudaSuccess;
+  const uint64_t tile = (uint64_t)g.ps * (uint64_t)g.D * 2;
+  const uint64_t stride = (tile + 127) / 128 * 128;
+  const uint64_t smem = (uint64_t)g.Hkv * stride;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaSuccess;
-  // the EP view of layer `layer` in every region: [region][half][row][head][element]
-  CUtensorMap map;
-  const cuuint64_t dims[5] = {(cuuint64_t)g.D, (cuuint64_t)g.Hkv, (cuuint64_t)g.pages_ep * (cuuint64_t)g.ps, 2,
+  // the EP view of layer `layer` in every region, one map per half (K, V):
+  // [region][page][row in page][head][element]
+  CUtensorMap map[2];
+  const cuuint64_t dims[5] = {(cuuint64_t)g.D, (cuuint64_t)g.Hkv, (cuuint64_t)g.ps, (cuuint64_t)g.pages_ep,
                               (cuuint64_t)g.P};
-  const cuuint64_t strides[4] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.Hkv * g.D * 2, (cuuint64_t)g.kv_v_off,
-                                 (cuuint64_t)g.region_stride};
+  const cuuint64_t row = (cuuint64_t)g.Hkv * g.D * 2;
+  const cuuint64_t strides[4] = {(cuuint64_t)g.D * 2, row, row * (cuuint64_t)g.ps, (cuuint64_t)g.region_stride};
   const cuuint32_t box[5] = {(cuuint32_t)g.D, 1, (cuuint32_t)g.ps, 1, 1};
   const cuuint32_t unit[5] = {1, 1, 1, 1, 1};
-  void* ep_slot = g.base + g.kvslots_off + (uint64_t)(layer + 1) * g.kvslot_stride;
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, ep_slot, dims, strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaSuccess;
+  uint8_t* const ep_slot = g.base + g.kvslots_off + (uint64_t)(layer + 1) * g.kvslot_stride;
+  for (int c = 0; c < 2; ++c)
+    if (encode(&map[c], CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, ep_slot + (uint64_t)c * g.kv_v_off, dims, strides, box,
+               unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaSuccess;
   TmaKVParams t;
   t.base = g.base;
   t.desc = p.desc;
@@ -340,6 +382,7 @@ cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t
   t.tile_bytes = (uint32_t)tile;
   t.tile_stride = (uint32_t)stride;
   t.row_bytes = (uint32_t)g.D * 2;
+  t.stall_polls = stall_polls;
   t.pages_tp = g.pages_tp;
   t.span = g.regions();
   cudaLaunchConfig_t cfg = {};
@@ -353,7 +396,7 @@ cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t
   cfg.attrs = attr;
   cfg.numAttrs = chained ? 1 : 0;
   *done = true;
-  return cudaLaunchKernelEx(&cfg, kv_copy_ep2tp_tma, map, t);
+  return cudaLaunchKernelEx(&cfg, kv_copy_ep2tp_tma, map[0], map[1], t);
 }
 
 namespace {
@@ -386,13 +429,17 @@ cudaError_t run_copy(const KVParams& p, int dir, int64_t max_desc, cudaStream_t 
 }
 }  // namespace
 
+int kv_vector_bytes(const Geo& g) {
+  if (g.D % 16 == 0) return 32;
+  if (g.D % 8 == 0) return 16;
+  if (g.D % 4 == 0) return 8;
+  if (g.D % 2 == 0) return 4;
+  return 2;
+}
+
 cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_t max_desc, int use_sched,
-                           unsigned int call, cudaStream_t s, bool chained, bool allow_tma) {
-  int VB = 2;
-  if (g.D % 16 == 0) VB = 32;
-  else if (g.D % 8 == 0) VB = 16;
-  else if (g.D % 4 == 0) VB = 8;
-  else if (g.D % 2 == 0) VB = 4;
+                           unsigned int call, cudaStream_t s, bool chained, bool allow_tma, uint32_t stall_polls) {
+  const int VB = kv_vector_bytes(g);
   const uint32_t per = (uint32_t)VB / 2;
   const uint32_t Dv = (uint32_t)g.D / per;
   KVParams p;
@@ -422,7 +469,7 @@ cudaError_t launch_kv_copy(const Geo& g, const Ws& w, int dir, int layer, int64_
   p.span = g.regions();
   if (dir == 0 && allow_tma) {
     bool done = false;
-    const cudaError_t e = launch_ep2tp_tma(g, p, layer, max_desc, s, chained, &done);
+    const cudaError_t e = launch_ep2tp_tma(g, p, layer, max_desc, s, chained, stall_polls, &done);
     if (done || e != cudaSuccess) return e;
   }
   switch (VB) {

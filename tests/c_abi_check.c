@@ -28,7 +28,8 @@ int main(void) {
       (any_fn)reshard_kv_tp2ep_staged, (any_fn)reshard_attn_ep2tp, (any_fn)reshard_attn_tp2ep,
       (any_fn)umm_get_attn_mode, (any_fn)umm_set_attn_mode, (any_fn)umm_switch_ep2tp,
       (any_fn)umm_switch_tp2ep, (any_fn)umm_policy_create, (any_fn)umm_policy_destroy,
-      (any_fn)umm_policy_step, (any_fn)umm_policy_state, (any_fn)umm_set_switch_overlap};
+      (any_fn)umm_policy_step, (any_fn)umm_policy_state, (any_fn)umm_set_switch_overlap,
+      (any_fn)umm_kv_copy_kernel, (any_fn)umm_test_stall_tma_wait};
   for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i)
     if (!fns[i]) return 10;
   printf("entry_points %zu\n", sizeof(fns) / sizeof(fns[0]));
@@ -61,6 +62,12 @@ int main(void) {
   printf("bad_heads %d\n", umm_required_bytes(&bad, &bytes));
   printf("null_handle %d\n", reshard_weights_ep2tp(NULL, NULL));
   printf("strerror_capacity %s\n", umm_strerror(UMM_ERR_CAPACITY));
+  int32_t kern = -1, vbytes = -1;
+  printf("kv_copy_ep2tp_rc %d\n", umm_kv_copy_kernel(&d, 0, &kern, &vbytes));
+  printf("kv_copy_ep2tp %d %d\n", kern, vbytes);
+  printf("kv_copy_tp2ep_rc %d\n", umm_kv_copy_kernel(&d, 1, &kern, &vbytes));
+  printf("kv_copy_tp2ep %d %d\n", kern, vbytes);
+  printf("stall_hook_null %d\n", umm_test_stall_tma_wait(NULL, 0, 1));
 
   /* the switch policy (host C++): a burst above T_h switches to EP */
   umm_policy_params pp;

@@ -182,6 +182,12 @@ def test_c_program_uses_the_abi(umm, tmp_path):
     assert int(got["bad_heads"]) == umm.UMM_ERR_INVALID_ARG
     assert int(got["null_handle"]) == umm.UMM_ERR_INVALID_ARG
     assert got["strerror_capacity"] == umm.strerror(umm.UMM_ERR_CAPACITY)
+    assert int(got["kv_copy_ep2tp_rc"]) == umm.UMM_OK and int(got["kv_copy_tp2ep_rc"]) == umm.UMM_OK
+    assert tuple(int(x) for x in got["kv_copy_ep2tp"].split()) == umm.umm_kv_copy_kernel(dims, 0) == \
+        (umm.UMM_KV_COPY_TMA, 0)
+    assert tuple(int(x) for x in got["kv_copy_tp2ep"].split()) == umm.umm_kv_copy_kernel(dims, 1) == \
+        (umm.UMM_KV_COPY_LSU, 32)
+    assert int(got["stall_hook_null"]) == umm.UMM_ERR_INVALID_ARG
     assert (int(got["policy_last_decision"]), int(got["policy_mode"]), int(got["policy_switches"])) == \
         (umm.POLICY_TO_EP, umm.UMM_MODE_EP, 1)
 
@@ -275,3 +281,71 @@ def test_binding_refuses_arrays_that_cannot_be_the_kernels_input(umm, monkeypatc
     with pytest.raises(umm.UmmError):
         umm.umm_create(lib_dims(umm, TINY), torch.zeros(64, dtype=torch.uint8), 64)
     assert spy.calls == ["reshard_kv_ep2tp"] * 3 + ["umm_assign_pages", "umm_switch_tp2ep"]
+
+
+def _kv_dims(umm, P, Hkv, D, ps, pages_tp):
+    return umm.make_dims(P=P, N=1, Hkv=Hkv, D=D, ps=ps, pages_tp=pages_tp, max_requests=16, max_pages=1024)
+
+
+@pytest.mark.parametrize("ps,pages_tp", [(1, 2**31 - 1), (2, 2**30), (16, 2**27), (16, 2**27 + 64),
+                                         (256, 2**27), (16, 2**31 - 16)])
+def test_tma_copy_addresses_pages_not_rows(umm, ps, pages_tp):
+    """The TMA KV EP->TP copy addresses an EP page by its page id (tensor
+    coordinates {element, head, row in page, page, region}), so EP pools of
+    2^31 - 1, 2^31 and more token rows (pages x page size) keep the TMA copy:
+    no coordinate is ever page * page_size.  Every pool the handle accepts has
+    page ids below 2^31, and one page more is refused."""
+    d = _kv_dims(umm, 1, 1, 8, ps, pages_tp)
+    L = umm.umm_layout_for_dims(d)
+    assert L["pages_ep"] == pages_tp and L["pages_ep"] < 2**31
+    assert umm.umm_kv_copy_kernel(d, 0) == (umm.UMM_KV_COPY_TMA, 0)
+    assert umm.umm_kv_copy_kernel(d, 1) == (umm.UMM_KV_COPY_LSU, 16)
+
+
+def test_page_ids_are_capped_below_2_31(umm):
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_required_bytes(_kv_dims(umm, 1, 1, 8, 16, 2**31))
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_kv_copy_kernel(_kv_dims(umm, 1, 1, 8, 16, 2**31), 0)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("P,Hkv,D,ps,want", [
+    (8, 4, 128, 16, ("TMA", 0)),      # the full-switch shape: one head per TP rank
+    (2, 2, 16, 16, ("TMA", 0)),
+    (2, 4, 128, 16, ("LSU", 32)),     # two heads per TP rank
+    (8, 4, 4, 16, ("LSU", 8)),        # 8-byte head rows: not a bulk-copy size
+    (8, 4, 12, 16, ("LSU", 8)),       # 24-byte head rows
+    (4, 4, 256, 32, ("LSU", 32)),     # 4 heads x 16 KiB tiles: over 48 KiB of shared memory
+    (8, 1, 128, 512, ("LSU", 32)),    # a 512-row page: over the 256 box limit
+    (3, 1, 5, 16, ("LSU", 2)),
+])
+def test_kv_copy_kernel_choice(umm, P, Hkv, D, ps, want):
+    d = _kv_dims(umm, P, Hkv, D, ps, 64 * max(1, Hkv // max(1, Hkv // P)))
+    k, vb = umm.umm_kv_copy_kernel(d, 0)
+    assert ({umm.UMM_KV_COPY_TMA: "TMA", umm.UMM_KV_COPY_LSU: "LSU"}[k], vb) == want
+    assert umm.umm_kv_copy_kernel(d, 1)[0] == umm.UMM_KV_COPY_LSU
+
+
+def test_kv_copy_kernel_bad_arguments(umm):
+    d = _kv_dims(umm, 8, 4, 128, 16, 64)
+    for bad in (2, -1):
+        with pytest.raises(umm.UmmError) as ei:
+            umm.umm_kv_copy_kernel(d, bad)
+        assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_kv_copy_kernel(umm.make_dims(P=8, E=8, H=8, I=8), 0)      # no KV cache
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+
+
+def test_stall_hook_is_checked_build_only(umm):
+    """The normal build refuses the TMA-wait test hook; the checked build
+    accepts it only for a handle (the GPU test drives it)."""
+    with pytest.raises(umm.UmmError) as ei:
+        umm.umm_test_stall_tma_wait(0x1, 0, 64)
+    assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    with umm.checked_library():
+        with pytest.raises(umm.UmmError) as ei:
+            umm.umm_test_stall_tma_wait(None, 0, 64)
+        assert ei.value.code == umm.UMM_ERR_INVALID_ARG

@@ -90,3 +90,70 @@ def test_access_flag_reported_and_cleared():
         assert dev.status() == (0, 0)
         assert np.all(dev.buf[st_off:st_off + 8].cpu().numpy() == 0)
         dev.close()
+
+
+@pytest.mark.parametrize("N", [2, 3])
+def test_tma_wait_runs_out_on_the_device(N):
+    """The bounded mbarrier wait of the TMA KV copy, made to run out on the
+    GPU (checked-build hook umm_test_stall_tma_wait): every CTA of the call's
+    last layer, after its tensor loads have landed, waits on a barrier that
+    never completes, gives up after 64 polls and takes the timeout exit with
+    no copy in flight.  Then:
+      - umm_status_sync reports UMM_ERR_TIMEOUT (flag TIMEOUT only), and the
+        KV mode stays TP (the call ran, incomplete);
+      - a validating kernel enqueued after the call did nothing;
+      - exactly the earlier layers were copied: the buffer equals its initial
+        contents with the TP slots of those layers taken from the oracle's
+        complete EP->TP, and nothing else written;
+      - the handle recovers: once the flag is read, a new EP->TP call (the
+        cache rebuilt first when a copied layer overwrote an EP slot) equals
+        the oracle."""
+    from gpu_helpers import fill_device, i32
+    from helpers import initial_kv_state, kvslot
+    import oracle
+    w = TINY.with_(N=N)
+    dev = DevUMM(w, seed=4)
+    assert umm.umm_kv_copy_kernel(dev.dims, 0)[0] == umm.UMM_KV_COPY_TMA
+    st = initial_kv_state(w, dev.d, dev.L, seed=4)
+    R, maxp = len(st.lens), st.ep_pt.shape[1]
+    args = (R, maxp, i32(st.lens), i32(st.owner), i32(st.ep_pt), i32(st.tp_pt))
+    ref0 = dev.host()
+    full = ref0.copy()
+    assert oracle.kv_ep2tp(full, dev.d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    L, d = dev.L, dev.d
+    umm.umm_test_stall_tma_wait(dev.h, N - 1, 64)
+    umm.reshard_kv_ep2tp(dev.h, *args)
+    tp_pos = torch.full((R,), -3, dtype=torch.int32, device="cuda")
+    umm.gather_requests_ep2tp(dev.h, R, i32(st.owner), tp_pos)
+    torch.cuda.synchronize()
+    assert dev.status() == (umm.UMM_ERR_TIMEOUT, umm.FLAG_TIMEOUT)
+    assert umm.umm_get_modes(dev.h)[1] == umm.UMM_MODE_TP
+    assert (tp_pos.cpu() == -3).all()
+    want = ref0.copy()
+    for q in range(d.P):
+        for layer in range(N - 1):
+            a = kvslot(L, q, layer, 0)
+            want[a:a + L["kvslot_stride"]] = full[a:a + L["kvslot_stride"]]
+    np.testing.assert_array_equal(dev.host(), want)
+    # recovery: the hook off, the flag read; the cache rebuilt when a copied
+    # layer (l >= 1) overwrote EP slot l, then EP->TP again
+    umm.umm_test_stall_tma_wait(dev.h, -1, 0)
+    assert dev.status() == (0, 0)
+    if N > 2:
+        fill_device(dev.buf, L, w, 4)
+    umm.umm_set_modes(dev.h, umm.UMM_MODE_EP, umm.UMM_MODE_EP)
+    umm.reshard_kv_ep2tp(dev.h, *args)
+    torch.cuda.synchronize()
+    assert dev.status() == (0, 0)
+    np.testing.assert_array_equal(dev.host(), full)
+    dev.close()
+
+
+def test_tma_wait_hook_range():
+    dev = DevUMM(TINY, seed=4, fill=False)
+    for bad in (-2, TINY.N):
+        with pytest.raises(umm.UmmError) as ei:
+            umm.umm_test_stall_tma_wait(dev.h, bad, 64)
+        assert ei.value.code == umm.UMM_ERR_INVALID_ARG
+    umm.umm_test_stall_tma_wait(dev.h, 0, 0)       # polls 0: off
+    dev.close()
