@@ -82,7 +82,8 @@ extern "C" {
 #define UMM_ERR_CUDA         6  /* a CUDA runtime call failed (a launch of a multi-kernel
                                    call: the kernels enqueued before it stay enqueued)    */
 #define UMM_ERR_TIMEOUT      7  /* a bounded device wait (the mbarrier of a TMA copy) gave
-                                   up: that layer copy is incomplete                      */
+                                   up: that layer copy is incomplete and the KV cache is in
+                                   no complete layout (see reshard_kv_ep2tp)              */
 #define UMM_ERR_DUP_PAGE     8  /* two live pages would be written to one destination page */
 #define UMM_ERR_BAD_REQUEST  9  /* length < 0 or > max_pages_per_req*page_size, owner or
                                    list position out of range                             */
@@ -263,8 +264,9 @@ int place_requests_tp2ep(umm_t* u, int32_t R, const int32_t* d_seq_lens, const i
  * not be entered (inside allocator callbacks, under a strict memory budget,
  * while other work is being captured), cannot provide one.  This variant takes
  * no handle and allocates nothing: its scratch (the list-position -> request
- * map) is a fixed 64 KiB array of this library's own device memory, which
- * every GPU that loads the library reserves until the process exits.
+ * map and the rank chosen per sorted position) is two fixed arrays of this
+ * library's own device memory, 80 KiB together, which a GPU keeps from this
+ * entry point's first call on it until the process exits.
  *  - P in [1, 64]; R in [0, 16384]: a larger R is refused with
  *    UMM_ERR_CAPACITY before anything is enqueued.
  *  - Same arguments and results as place_requests_tp2ep(); d_status (device
@@ -273,9 +275,12 @@ int place_requests_tp2ep(umm_t* u, int32_t R, const int32_t* d_seq_lens, const i
  *    untouched).  With R == 0 nothing is enqueued and d_status is not written.
  *  - All calls on one GPU share the scratch array: calls whose kernels may
  *    overlap on the GPU (unordered streams) race; order them on one stream.
- *  - The first call on each device looks up the array's address and sets the
- *    kernel's shared-memory limit (no allocation); make that call before any
- *    stream capture. */
+ *  - The first call on each device (R == 0 included) does the set-up: it
+ *    looks up the arrays' addresses and sets the kernel's shared-memory
+ *    limit.  Under CUDA's lazy module loading (the default), this is when the
+ *    driver loads the entry point's device code and arrays onto the device,
+ *    which may take device memory.  Make that first call at start-up, before
+ *    any stream capture; later calls take no device memory. */
 int place_requests_tp2ep_noalloc(int32_t P, int32_t R, const int32_t* d_seq_lens, const int32_t* d_list_pos,
                                  int32_t* d_owner, int32_t* d_local_pos, int32_t* d_status, void* stream);
 
@@ -307,7 +312,18 @@ int umm_assign_pages(umm_t* u, int32_t npools, int32_t R, const int32_t* d_seq_l
  * and bulk stores write its live rows to each replica.  Errors: MODE,
  * INVALID_ARG (sync); BAD_REQUEST, CAPACITY, PAGE_OOB, DUP_PAGE (device,
  * before any write); TIMEOUT (the TMA copy's bounded wait gave up; not
- * expected). */
+ * expected).  After TIMEOUT: the layers before the one whose wait ran out
+ * were copied; a CTA whose wait ran out stored nothing, other CTAs of that
+ * layer may have stored their pages; the next layer may have copied pages
+ * too if it had started under programmatic dependent launch before the flag
+ * was raised; later layers stored nothing.  The handle stays usable
+ * (umm_status_sync() clears the flag), but the KV cache must be rebuilt or
+ * reloaded by the caller, who then declares its layout with umm_set_modes().
+ * A CTA waits for its own loads at most twice (each a bounded number of
+ * polls) before it leaves; should both run out, a load may still write that
+ * CTA's shared memory after it has exited.  Tensor-map coordinates are
+ * {element, head, row in page, page, region}, each below 2^31 for every
+ * accepted pool size. */
 int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
                      const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
                      const int32_t* d_tp_page_table, void* stream);
@@ -319,6 +335,33 @@ int reshard_kv_ep2tp(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
 int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32_t* d_seq_lens,
                      const int32_t* d_ep_owner, const int32_t* d_ep_page_table,
                      const int32_t* d_tp_page_table, void* stream);
+
+/* Which copy kernel a KV reshard of `dims` launches per layer (host-only;
+ * no GPU needed).  dir 0 = EP->TP, 1 = TP->EP.  *kernel = UMM_KV_COPY_TMA
+ * (EP->TP through tensor-map loads and bulk stores, see reshard_kv_ep2tp) or
+ * UMM_KV_COPY_LSU (vector loads and stores with 64-bit offsets);
+ * *vector_bytes (may be NULL) receives the LSU copy's vector width, 0 for
+ * TMA.  This is the shape's choice: reshard_kv_ep2tp still runs the LSU copy
+ * when the driver cannot encode the tensor map, and so does a one-call
+ * switch whose weight copies run on the side stream (umm_set_switch_overlap).
+ * Errors: INVALID_ARG (bad dims, no KV cache, bad dir, kernel NULL). */
+#define UMM_KV_COPY_LSU 0
+#define UMM_KV_COPY_TMA 1
+int umm_kv_copy_kernel(const umm_dims* dims, int32_t dir, int32_t* kernel, int32_t* vector_bytes);
+
+/* Test hook of the checked build (libumm_checked.so; libumm.so returns
+ * UMM_ERR_INVALID_ARG and does nothing).  From the next KV EP->TP call of
+ * this handle on, every CTA of the TMA copy of layer `layer` makes, once its
+ * tensor loads have landed, one more wait on a barrier that never completes,
+ * limited to `polls` polls.  That wait runs out and the CTA takes the exit of
+ * a timed-out wait with no copy in flight: it raises UMM_FLAG_TIMEOUT and
+ * stores nothing.  Kernels enqueued after the call see the flag and do
+ * nothing until umm_status_sync() reports UMM_ERR_TIMEOUT.  With `layer` the
+ * call's last layer, exactly the earlier layers are copied (see
+ * reshard_kv_ep2tp for a layer in the middle).  layer = -1 or polls = 0
+ * turns it off.
+ * Errors: INVALID_ARG (layer outside [-1, num_layers), or libumm.so). */
+int umm_test_stall_tma_wait(umm_t* u, int32_t layer, uint32_t polls);
 
 /* The staged (collective-style) KV reshard, for comparison with the fused
  * one (§3.2: gather scattered token slots into per-peer contiguous blocks,
@@ -385,7 +428,8 @@ int umm_kv_check_capacity(const umm_t* u, int32_t target_kv_mode, int32_t R,
  * CAPACITY > PAGE_OOB > DUP_PAGE; UMM_OK if none) in *status_out (flags in
  * *flags_out, may be NULL).  If a KV reshard was stopped by a validation
  * flag, the handle's KV mode is set back to the layout the data is actually
- * in; ACCESS and TIMEOUT leave it (that reshard ran, with a copy missing). */
+ * in; ACCESS and TIMEOUT leave it (that reshard ran, with copies missing: see
+ * reshard_kv_ep2tp for what TIMEOUT leaves behind). */
 int umm_status_sync(umm_t* u, void* stream, int32_t* status_out, uint32_t* flags_out);
 
 /* Static description of a status code. */
