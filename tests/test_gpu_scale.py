@@ -4,8 +4,10 @@ cannot hold these buffers, so outputs are checked (a) on random samples the
 oracle maps one by one (its element maps + the generator's value at the
 source), (b) whole, against properties that hold at any size: the TP shards
 equal torch slices of the full EP tensors (§3.1 shapes), the EP->TP->EP
-round trip is the identity (weights), and every live KV row of a few whole
-requests, and (c) bytes outside every destination keep their contents."""
+round trip is the identity (weights), and (c) every byte of every KV slot of
+every region, after each direction, against contents rebuilt on the device
+from the generator and the oracle's page tables (KVComplete), and bytes
+outside every destination keep their contents."""
 from __future__ import annotations
 
 import numpy as np
@@ -229,54 +231,157 @@ def _check_kv_tp2ep(run: KVRun, rng):
     np.testing.assert_array_equal(_gather(dev, dst // 2), _expect(dev, src // 2, True))
 
 
-def _check_kv_whole_requests(run: KVRun, ks):
-    """Every live row of a few whole requests (all layers, K and V, all
-    heads) under TP, against the generator at their EP source rows."""
-    dev, w, L = run.dev, run.dev.w, run.dev.L
-    u = dev.u16()
-    hd = w.D
-    for k in ks:
-        n = int(run.lens[k])
-        t = np.arange(n)
+class KVComplete:
+    """Every byte of every KV slot of every region, compared whole.
+
+    The expected contents are rebuilt on the device, one (slot, half) at a
+    time: the generator's initial values, with the rows each switch writes
+    replaced by the generator's values at their sources (§3.2, Fig. 5: the
+    page table maps logical page p of request k to a physical page; token t
+    is row t % page_size of page table[k][t // page_size]; §4.2 Fig. 7: EP
+    layer l in slot l+1, TP layer l in slot l).  Sources and destinations are
+    the oracle's (owners, page tables); the row arithmetic below is pinned to
+    the oracle's element map (kv_elem) on a sample before it is used.
+
+    After EP->TP, slot l (l < N) of rank q holds TP layer l: its initial bytes
+    with every live token row of TP page tp_pt[k][p] set to the row of the
+    request's EP page in EP slot l+1 of its owner, heads of rank q only; slot
+    N is untouched.  After TP->EP, slot l+1 holds that state (TP layer l+1
+    for l+1 < N, else the initial bytes) with every live row of new EP page
+    ep_pt1[k][p] of the new owner set to the original EP row; slot 0 keeps TP
+    layer 0.  The page tails, unused pages and alignment padding of each slot
+    are compared too: they must keep their initial bytes."""
+
+    def __init__(self, run: KVRun, samples: int = 20_000):
+        dev, w, L = run.dev, run.dev.w, run.dev.L
+        self.run, self.dev, self.w, self.L = run, dev, w, L
+        P, ps = w.P, w.ps
+        lens = run.lens.astype(np.int64)
+        k = np.repeat(np.arange(run.R), lens)
+        t = np.arange(len(k)) - np.repeat(np.cumsum(lens) - lens, lens)
+        p, row = t // ps, t % ps
+        o0, o1 = run.owner0[k].astype(np.int64), run.owner1[k].astype(np.int64)
+        src0 = run.ep_pt0[k, p].astype(np.int64) * ps + row
+        tp = run.tp_pt[k, p].astype(np.int64) * ps + row
+        dst1 = run.ep_pt1[k, p].astype(np.int64) * ps + row
+        self.half_u16 = L["pages_tp"] * ps * L["h_tp"] * w.D
+        assert self.half_u16 == L["pages_ep"] * ps * w.Hkv * w.D
+        self._pin(k, t, o0, o1, src0, tp, dst1, samples)
+        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.by_o0 = {r: (dv(src0[o0 == r]), dv(tp[o0 == r])) for r in range(P)}
+        self.by_move = {(a, b): (dv(src0[(o0 == a) & (o1 == b)]), dv(dst1[(o0 == a) & (o1 == b)]))
+                        for a in range(P) for b in range(P)}
+        self.heads = [heads_of_rank(P, w.Hkv, q) for q in range(P)]
+
+    def slot_off(self, r: int, s: int) -> int:
+        L = self.L
+        return r * L["region_stride"] + L["kvslots_off"] + s * L["kvslot_stride"]
+
+    def _pin(self, k, t, o0, o1, src0, tp, dst1, n):
+        """The flat element offsets used below equal the oracle's kv_elem."""
+        run, w, L, d = self.run, self.w, self.L, self.dev.d
+        rng = np.random.default_rng(17)
+        pick = rng.integers(0, len(k), n)
+        c = rng.integers(0, 2, n)
+        h = rng.integers(0, w.Hkv, n)
+        e = rng.integers(0, w.D, n)
+        layer = rng.integers(0, w.N, n)
+        for i in range(n):
+            j = int(pick[i])
+            q = next(q for q in range(w.P) if h[i] in self.heads_of(q))
+            hl = self.heads_of(q).index(int(h[i]))
+            pg, tt = divmod(int(t[j]), w.ps)
+            kk = int(k[j])
+            a, b = oracle.kv_elem(d, int(o0[j]), q, int(run.ep_pt0[kk, pg]), int(run.tp_pt[kk, pg]), tt,
+                                  int(c[i]), int(h[i]), int(e[i]), int(layer[i]) + 1, int(layer[i]))
+            ep = self.slot_off(int(o0[j]), int(layer[i]) + 1) + c[i] * L["kv_v_off"] + \
+                2 * ((int(src0[j]) * w.Hkv + int(h[i])) * w.D + int(e[i]))
+            tpo = self.slot_off(q, int(layer[i])) + c[i] * L["kv_v_off"] + \
+                2 * ((int(tp[j]) * L["h_tp"] + hl) * w.D + int(e[i]))
+            assert (a, b) == (ep, tpo), i
+            a1, _ = oracle.kv_elem(d, int(o1[j]), q, int(run.ep_pt1[kk, pg]), 0, tt, int(c[i]), int(h[i]),
+                                   int(e[i]), int(layer[i]) + 1, 0)
+            assert a1 == self.slot_off(int(o1[j]), int(layer[i]) + 1) + c[i] * L["kv_v_off"] + \
+                2 * ((int(dst1[j]) * w.Hkv + int(h[i])) * w.D + int(e[i])), i
+
+    def heads_of(self, q: int) -> list[int]:
+        return heads_of_rank(self.w.P, self.w.Hkv, q)
+
+    def _half(self, r: int, s: int, c: int) -> int:
+        return (self.slot_off(r, s) + c * self.L["kv_v_off"]) // 2
+
+    def got(self, r: int, s: int, c: int) -> torch.Tensor:
+        o = self._half(r, s, c)
+        return self.dev.u16()[o:o + self.half_u16]
+
+    def initial(self, r: int, s: int, c: int) -> torch.Tensor:
+        return _regen(self.dev, 2 * self._half(r, s, c), 2 * self.half_u16, True)
+
+    def _tp_rows(self, exp: list, layer: int, c: int) -> None:
+        """Write TP layer `layer` (from EP slot layer+1) into exp[q] (TP view)."""
+        w, h_tp = self.w, self.L["h_tp"]
+        for r in range(w.P):
+            s_idx, t_idx = self.by_o0[r]
+            if not len(s_idx):
+                continue
+            vals = self.initial(r, layer + 1, c).view(-1, w.Hkv, w.D)[s_idx]
+            for q in range(w.P):
+                exp[q].view(-1, h_tp, w.D)[t_idx] = vals[:, self.heads[q], :]
+            del vals
+
+    def _pads_intact(self, r: int, s: int) -> None:
+        """Alignment padding after each half of a KV slot keeps its bytes."""
+        L, u = self.L, self.dev.u16()
+        for a, b in ((self.half_u16 * 2, L["kv_v_off"]), (L["kv_v_off"] + self.half_u16 * 2, L["kvslot_stride"])):
+            if b > a:
+                o = self.slot_off(r, s) + a
+                assert torch.equal(u[o // 2:(o + b - a) // 2], _regen(self.dev, o, b - a, True)), (r, s)
+
+    def check_after_ep2tp(self) -> None:
+        w = self.w
+        torch.cuda.empty_cache()
         for layer in range(w.N):
             for c in range(2):
-                ep_base = (int(run.owner0[k]) * L["region_stride"] + L["kvslots_off"] +
-                           (layer + 1) * L["kvslot_stride"] + c * L["kv_v_off"]) // 2
-                ep_rows = ep_base + (run.ep_pt0[k, t // w.ps].astype(np.int64) * w.ps + t % w.ps) * w.Hkv * hd
-                want = _expect(dev, (ep_rows[:, None] + np.arange(w.Hkv * hd)[None, :]).ravel(),
-                               True).reshape(n, w.Hkv, hd)
+                exp = [self.initial(q, layer, c) for q in range(w.P)]
+                self._tp_rows(exp, layer, c)
                 for q in range(w.P):
-                    heads = list(range(q * w.Hkv // w.P, (q + 1) * w.Hkv // w.P)) if w.Hkv >= w.P \
-                        else [q * w.Hkv // w.P]
-                    tp_base = (q * L["region_stride"] + L["kvslots_off"] + layer * L["kvslot_stride"] +
-                               c * L["kv_v_off"]) // 2
-                    tp_rows = tp_base + (run.tp_pt[k, t // w.ps].astype(np.int64) * w.ps + t % w.ps) * \
-                        L["h_tp"] * hd
-                    idx = torch.from_numpy((tp_rows[:, None] + np.arange(L["h_tp"] * hd)[None, :]).ravel()).cuda()
-                    got = u[idx].cpu().numpy().reshape(n, L["h_tp"], hd)
-                    np.testing.assert_array_equal(got, want[:, heads, :])
+                    assert torch.equal(self.got(q, layer, c), exp[q]), ("ep2tp", layer, c, q)
+                del exp
+        for r in range(w.P):
+            for c in range(2):
+                assert torch.equal(self.got(r, w.N, c), self.initial(r, w.N, c)), ("slot N", r, c)
+            for s in range(w.N + 1):
+                self._pads_intact(r, s)
+        torch.cuda.empty_cache()
 
-
-def _check_kv_untouched(run: KVRun, rng):
-    """TP slot 0 pages that no request uses, and the rows past the end of
-    every request's last page, keep their initial contents."""
-    dev, w, L = run.dev, run.dev.w, run.dev.L
-    used = np.zeros(L["pages_tp"], bool)
-    for k in range(run.R):
-        used[run.tp_pt[k, :int(synth.npages(run.lens[k:k + 1], w.ps)[0])]] = True
-    free_pages = np.flatnonzero(~used)
-    page_u16 = w.ps * L["h_tp"] * w.D
-    for pg in rng.choice(free_pages, size=min(64, len(free_pages)), replace=False):
-        for q in rng.choice(w.P, 2, replace=False):
-            base = (int(q) * L["region_stride"] + L["kvslots_off"]) // 2 + int(pg) * page_u16
-            idx = np.arange(base, base + page_u16)
-            np.testing.assert_array_equal(_gather(dev, idx), _expect(dev, idx, True))
-    tails = [k for k in range(run.R) if run.lens[k] % w.ps][:64]
-    for k in tails:
-        p = int(run.lens[k]) // w.ps
-        base = (L["kvslots_off"]) // 2 + int(run.tp_pt[k, p]) * page_u16
-        idx = np.arange(base + (int(run.lens[k]) % w.ps) * L["h_tp"] * w.D, base + page_u16)
-        np.testing.assert_array_equal(_gather(dev, idx), _expect(dev, idx, True))
+    def check_after_tp2ep(self) -> None:
+        w = self.w
+        torch.cuda.empty_cache()
+        for layer in range(w.N):
+            for c in range(2):
+                exp = [self.initial(r, layer + 1, c) for r in range(w.P)]
+                if layer + 1 < w.N:
+                    self._tp_rows(exp, layer + 1, c)
+                for a in range(w.P):
+                    src = self.initial(a, layer + 1, c).view(-1, w.Hkv, w.D)
+                    for b in range(w.P):
+                        s_idx, d_idx = self.by_move[(a, b)]
+                        if len(s_idx):
+                            exp[b].view(-1, w.Hkv, w.D)[d_idx] = src[s_idx]
+                    del src
+                for r in range(w.P):
+                    assert torch.equal(self.got(r, layer + 1, c), exp[r]), ("tp2ep", layer, c, r)
+                del exp
+        for c in range(2):
+            exp = [self.initial(q, 0, c) for q in range(w.P)]
+            self._tp_rows(exp, 0, c)
+            for q in range(w.P):
+                assert torch.equal(self.got(q, 0, c), exp[q]), ("slot 0", c, q)
+            del exp
+        for r in range(w.P):
+            for s in range(w.N + 1):
+                self._pads_intact(r, s)
+        torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("w,timed,overlap", [(KV_256REQ, False, False), (FULL_SWITCH, False, False),
@@ -293,18 +398,19 @@ def test_kv_and_full_switch_fullsize(w, timed, overlap):
     umm.umm_profile_enable(dev.h, timed)
     umm.umm_set_switch_overlap(dev.h, overlap)
     run = KVRun(dev)
+    full = KVComplete(run)
     rng = np.random.default_rng(1)
     switch = bool(w.E)
     run.ep2tp(switch)
     torch.cuda.synchronize()
     _check_kv_ep2tp(run, rng)
-    _check_kv_whole_requests(run, [int(np.argmax(run.lens)), int(np.argmin(run.lens)), 0])
-    _check_kv_untouched(run, rng)
+    full.check_after_ep2tp()
     if w.E:
         _check_weights_ep2tp(dev, rng)
     run.tp2ep(switch)
     torch.cuda.synchronize()
     _check_kv_tp2ep(run, rng)
+    full.check_after_tp2ep()
     if w.E:
         _check_weights_round_trip(dev)
     dev.close()
