@@ -42,7 +42,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
-from synth.workloads import ALL, FULL_SWITCH  # noqa: E402
+from synth.workloads import ALL, ATTN_QWEN3_SHAPE, FULL_SWITCH, KV_256REQ, WEIGHTS_H2048, WEIGHTS_H4096  # noqa: E402
 
 METRIC = "reshard GB/s (read+write) and % of HBM peak; ms per layer and per full switch"
 UNIT = "GB/s"
@@ -68,6 +68,9 @@ def parse():
                          "one JSON line each with ms per phase (weights, request metadata, descriptor pass, KV)")
     ap.add_argument("--no-ceilings", action="store_true",
                     help="skip the read:write-mix ceilings measured after the timed region")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (expert weights of two sizes, KV of 256 requests, "
+                         "attention weights) timed after the full switch for the `configs` object")
     ap.add_argument("--ceilings", action="store_true",
                     help="instead of the benchmark line: the HBM rate a plain streaming copy reaches for the "
                          "read:write mix of each reshard kernel, one JSON line per mix")
@@ -638,6 +641,61 @@ class CpuSample:
         return moved, secs
 
 
+LAYER_BYTES = (("weights_ep2tp", "weights_per_layer"), ("weights_tp2ep", "weights_per_layer"),
+               ("kv_ep2tp", "kv_ep2tp_per_layer"), ("kv_tp2ep", "kv_tp2ep_per_layer"),
+               ("attn_ep2tp", "attn_ep2tp_per_layer"), ("attn_tp2ep", "attn_tp2ep_per_layer"))
+
+
+def kernel_table(prof: dict, b: dict, peak: float, ceil: dict) -> dict:
+    """Per kernel kind timed: launches (layer copies or calls), ms per launch,
+    and for the copies GB/s of algorithmic bytes, its fraction of the measured
+    copy peak and of the plain-copy ceiling of the kernel's read:write mix."""
+    per_kind = {k: {"launches": n, "ms_per_launch": round(ms / n, 4) if n else None}
+                for k, (n, ms) in prof.items() if n}
+    for k, key in LAYER_BYTES:
+        if k in per_kind and b.get(key):
+            gbs = b[key] / (per_kind[k]["ms_per_launch"] / 1e3) / 1e9
+            per_kind[k]["GB_s"] = round(gbs, 1)
+            per_kind[k]["frac_of_peak"] = round(gbs / peak, 4)
+            if MIX_OF_KIND.get(k) in ceil:
+                per_kind[k]["mix_ceiling_GB_s"] = ceil[MIX_OF_KIND[k]]
+                per_kind[k]["frac_of_mix_ceiling"] = round(gbs / ceil[MIX_OF_KIND[k]], 4)
+    return per_kind
+
+
+# the workloads timed after the full switch, for the `configs` object
+OTHER_CONFIGS = (("weights_e128_h2048_i768", WEIGHTS_H2048), ("weights_e128_h4096_i1536", WEIGHTS_H4096),
+                 ("kv_256req_u1k-32k", KV_256REQ), ("attention_hq64_hkv4_h4096", ATTN_QWEN3_SHAPE))
+
+
+def other_configs(args, peak: float, ceil: dict) -> dict:
+    """The other workloads on the same GPU, one after the other (each its own
+    buffer), EP->TP->EP round trips timed exactly as the full switch: the
+    same calls, per-kernel events around each call's chain of layer copies."""
+    import copy
+    sub = copy.copy(args)
+    sub.no_graph = sub.no_staged = sub.no_e2e = True
+    sub.overlap = False
+    out = {}
+    for label, w in OTHER_CONFIGS:
+        r = run_umm(sub, 0, 1, int(os.environ.get("LOCAL_RANK", 0)), w=w)
+        b = r["bytes"]
+        n = args.steps
+        ms_rt = r["ms_total"] / n
+        gbs = b["step"] / (ms_rt / 1e3) / 1e9
+        kern = kernel_table(r["prof"], b, peak, ceil)
+        out[label] = {
+            "workload": w.name, "layers": w.N, "steps": n, "warmup": args.warmup,
+            "bytes_per_round_trip": b["step"], "ms_per_round_trip": round(ms_rt, 3),
+            "ms_per_switch": {"ep2tp": round(r["ms_ep2tp"], 3), "tp2ep": round(r["ms_tp2ep"], 3)},
+            "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "frac_of_8TBs_nominal": round(gbs / 8000.0, 4),
+            "ms_per_layer": {k: v["ms_per_launch"] for k, v in kern.items() if "GB_s" in v},
+            "kernels": {k: v for k, v in kern.items() if "GB_s" in v},
+            "tokens": b.get("tokens"), "clocks": r["clocks"]}
+    return out
+
+
 def cpu_baseline(w):
     """The oracle on all host cores, plus a smaller sample on one core."""
     threads = os.cpu_count() or 1
@@ -791,24 +849,12 @@ def main():
                    "weights_tp2ep": "weights_kernel"}.get(dom)
     traffic = committed_traffic(kernel_name, {"tokens": b.get("tokens"), "bytes": per_launch_bytes}) \
         if kernel_name else None
-    per_kind = {k: {"launches": n, "ms_per_launch": round(ms / n, 4) if n else None}
-                for k, (n, ms) in prof.items() if n}
-    for k, key in (("weights_ep2tp", "weights_per_layer"), ("weights_tp2ep", "weights_per_layer"),
-                   ("kv_ep2tp", "kv_ep2tp_per_layer"), ("kv_tp2ep", "kv_tp2ep_per_layer"),
-                   ("attn_ep2tp", "attn_ep2tp_per_layer"), ("attn_tp2ep", "attn_tp2ep_per_layer")):
-        if k in per_kind and b.get(key):
-            gbs = b[key] / (per_kind[k]["ms_per_launch"] / 1e3) / 1e9
-            per_kind[k]["GB_s"] = round(gbs, 1)
-            per_kind[k]["frac_of_peak"] = round(gbs / peak, 4)
     # the same kernels against a plain streaming copy of their own read:write
     # mix, measured on this GPU after the timed region (context beside peak)
+    ceil = {} if args.no_ceilings else {row["ceiling"]: row["GB_s"] for row in run_ceilings()}
+    per_kind = kernel_table(prof, b, peak, ceil)
     mix = None
-    if not args.no_ceilings:
-        ceil = {row["ceiling"]: row["GB_s"] for row in run_ceilings()}
-        for k, v in per_kind.items():
-            if "GB_s" in v and MIX_OF_KIND.get(k) in ceil:
-                v["mix_ceiling_GB_s"] = ceil[MIX_OF_KIND[k]]
-                v["frac_of_mix_ceiling"] = round(v["GB_s"] / ceil[MIX_OF_KIND[k]], 4)
+    if ceil:
         if MIX_OF_KIND.get(dom) in ceil:
             c = ceil[MIX_OF_KIND[dom]]
             mix = {"mix": MIX_OF_KIND[dom], "GB_s": c, "frac": round(achieved / c, 4),
@@ -837,6 +883,8 @@ def main():
         "clocks": r["clocks"], "gpu_launches": r["launches"],
         "e2e": r["e2e"],
     }
+    if not args.no_configs and world == 1 and args.workload == FULL_SWITCH.name:
+        line["configs"] = other_configs(args, peak, ceil)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(r["w"])
     print(json.dumps(line), flush=True)

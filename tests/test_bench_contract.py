@@ -122,3 +122,29 @@ def test_ceiling_program_compiles():
     from ep_tp_weight_gb300 import build as umm_build
     exe = umm_build.build_ceiling()
     assert os.path.exists(exe) and os.access(exe, os.X_OK)
+
+
+def test_kernel_table_rates_and_fractions():
+    """The per-kernel rows of the bench line (full switch and `configs`):
+    GB/s = algorithmic bytes of one layer copy / ms per layer, and its
+    fractions of the measured peak and of the kernel's mix ceiling."""
+    b = {"weights_per_layer": 2_000_000_000, "kv_ep2tp_per_layer": 6_000_000_000}
+    prof = {"weights_ep2tp": (4, 1.0), "kv_ep2tp": (8, 8.0), "place": (2, 0.2), "order": (0, 0.0)}
+    ceil = {"1R1W sequential": 8000.0, "1R2W shuffled reads": 6000.0}
+    t = bench.kernel_table(prof, b, 7000.0, ceil)
+    assert set(t) == {"weights_ep2tp", "kv_ep2tp", "place"}
+    w = t["weights_ep2tp"]
+    assert w["launches"] == 4 and w["ms_per_launch"] == 0.25
+    assert w["GB_s"] == 8000.0 and w["frac_of_peak"] == round(8000 / 7000, 4) and w["frac_of_mix_ceiling"] == 1.0
+    kv = t["kv_ep2tp"]
+    assert kv["GB_s"] == 6000.0 and kv["frac_of_mix_ceiling"] == 1.0
+    assert "GB_s" not in t["place"] and t["place"]["ms_per_launch"] == 0.1
+    assert "frac_of_mix_ceiling" not in bench.kernel_table(prof, b, 7000.0, {})["weights_ep2tp"]
+
+
+def test_configs_cover_the_other_workloads():
+    """The `configs` object times the expert-weight sizes, the 256-request KV
+    workload and the attention weights: every workload but the full switch
+    (the line's own value) and the tiny parity case."""
+    from synth.workloads import ATTN_QWEN3_SHAPE, KV_256REQ, WEIGHTS_H2048, WEIGHTS_H4096
+    assert [w for _, w in bench.OTHER_CONFIGS] == [WEIGHTS_H2048, WEIGHTS_H4096, KV_256REQ, ATTN_QWEN3_SHAPE]
