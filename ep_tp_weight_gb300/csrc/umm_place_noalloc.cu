@@ -6,20 +6,23 @@
 // device pointers by the serving engine, or code that runs while a CUDA graph
 // is being built or while an allocator must not be entered) has no such
 // buffer and may not call cudaMalloc itself.  This variant computes the same
-// result with its scratch in a fixed array of this library's own device
-// memory, reserved when the library is loaded.
+// result with its scratch in two fixed arrays of this library's own device
+// memory (statically sized `__device__` arrays, 80 KiB together).
 //
 // Limits and caveats:
 //  - at most kNoAllocMaxRequests (16,384) requests and P <= 64 ranks; larger
 //    calls are refused with UMM_ERR_CAPACITY / UMM_ERR_INVALID_ARG before
 //    anything is enqueued;
-//  - the scratch arrays (80 KiB) exist once per GPU that loads the library,
-//    for the life of the process, and every call on that GPU shares it: two
+//  - the scratch arrays exist once per GPU that uses this entry point, for
+//    the life of the process, and every call on that GPU shares them: two
 //    calls whose kernels overlap on the GPU (different streams without an
 //    ordering between them) race and may produce wrong results;
-//  - the first call on a device looks up the arrays' device addresses and
-//    raises the kernel's shared-memory limit (no allocation); make that first
-//    call before capturing a stream into a CUDA graph.
+//  - the first call on a device (R == 0 included) does the set-up: it looks
+//    up the arrays' device addresses and raises the kernel's shared-memory
+//    limit.  With CUDA's lazy module loading (the default), that is when the
+//    driver loads this file's device code and arrays onto the device, which
+//    may take device memory; make that first call at start-up, before any
+//    stream capture.  Later calls take no device memory.
 #include <mutex>
 
 #include "umm_place.cuh"
