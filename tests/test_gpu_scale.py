@@ -354,6 +354,35 @@ class KVComplete:
                 self._pads_intact(r, s)
         torch.cuda.empty_cache()
 
+    def check_live_ep(self, owner, ep_pt) -> None:
+        """Every live element of every layer sits in EP page ep_pt[k][p] of
+        owner[k] with its original value (the generator's value at the
+        request's starting EP row: owner0, ep_pt0).  Bytes outside live rows
+        are not compared here."""
+        w, run, ps = self.w, self.run, self.w.ps
+        lens = run.lens.astype(np.int64)
+        k = np.repeat(np.arange(run.R), lens)
+        t = np.arange(len(k)) - np.repeat(np.cumsum(lens) - lens, lens)
+        p, row = t // ps, t % ps
+        o0, ot = run.owner0[k].astype(np.int64), np.asarray(owner)[k].astype(np.int64)
+        src0 = run.ep_pt0[k, p].astype(np.int64) * ps + row
+        dst = np.asarray(ep_pt)[k, p].astype(np.int64) * ps + row
+        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        moves = {(a, b): (dv(src0[(o0 == a) & (ot == b)]), dv(dst[(o0 == a) & (ot == b)]))
+                 for a in range(w.P) for b in range(w.P)}
+        torch.cuda.empty_cache()
+        for layer in range(w.N):
+            for c in range(2):
+                for a in range(w.P):
+                    src = self.initial(a, layer + 1, c).view(-1, w.Hkv, w.D)
+                    for b in range(w.P):
+                        s_idx, d_idx = moves[(a, b)]
+                        if len(s_idx):
+                            got = self.got(b, layer + 1, c).view(-1, w.Hkv, w.D)[d_idx]
+                            assert torch.equal(got, src[s_idx]), ("live", layer, c, a, b)
+                    del src
+        torch.cuda.empty_cache()
+
     def check_after_tp2ep(self) -> None:
         w = self.w
         torch.cuda.empty_cache()
@@ -420,8 +449,9 @@ def test_full_switch_soak_100_round_trips():
     """100 round trips of the full switch through umm_switch_*, on one handle,
     with new free lists on every trip (pages move each time).  Afterwards
     every weight slot that holds an EP layer is bit-identical to its start,
-    and sampled KV elements of every layer sit in their requests' final EP
-    pages with their original values."""
+    and every live KV element of every layer (and, independently, 200k
+    oracle-mapped samples) sits in its request's final EP page with its
+    original value."""
     w = FULL_SWITCH
     dev = DevUMM(w, seed=w.seed)
     run = KVRun(dev)
@@ -455,6 +485,7 @@ def test_full_switch_soak_100_round_trips():
         dst[i], _ = oracle.kv_elem(d, int(owner_t[k[i]]), int(q0[i]), int(ep_pt_t[k[i], p]), 0, t,
                                    int(c[i]), int(hh[i]), int(e[i]), int(layer[i]) + 1, 0)
     np.testing.assert_array_equal(_gather(dev, dst // 2), _expect(dev, src // 2, True))
+    KVComplete(run, samples=2_000).check_live_ep(owner_t, ep_pt_t)
     dev.close()
 
 
