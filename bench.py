@@ -401,6 +401,7 @@ def run_umm(args, rank, world, local_rank, w=None):
         raise RuntimeError(f"timed steps failed: {umm.strerror(st[0])}")
     ms_ep2tp = statistics.mean(a.elapsed_time(b) for a, b, _ in ev_half)
     ms_tp2ep = statistics.mean(b.elapsed_time(c) for _, b, c in ev_half)
+    step_ms = [a.elapsed_time(c) for a, _, c in ev_half]
     ms_total = max_over_ranks(ms_total, dev)
 
     # ---------------- the same round trip replayed from a CUDA graph
@@ -536,7 +537,8 @@ def run_umm(args, rank, world, local_rank, w=None):
     del buf
     torch.cuda.empty_cache()
     return dict(w=w, lens=lens_h, ms_total=ms_total, graph=graph, staged=staged, launches=launches, prof=prof, clocks=clk.summary(),
-                ms_ep2tp=ms_ep2tp, ms_tp2ep=ms_tp2ep, bytes=bytes_model, e2e=e2e, layout=L, nbytes=nbytes)
+                ms_ep2tp=ms_ep2tp, ms_tp2ep=ms_tp2ep, bytes=bytes_model, e2e=e2e, layout=L, nbytes=nbytes,
+                step_ms=step_ms)
 
 
 # ----------------------------------------------------------------------------- CPU oracle sample
@@ -865,6 +867,9 @@ def main():
         "vs_baseline": None, "dtype": "u16", "data": "synthetic (seeded; bf16 N(0,0.02) weights, N(0,1) KV)",
         "config": config,
         "ms_per_switch": {"ep2tp": round(r["ms_ep2tp"], 3), "tp2ep": round(r["ms_tp2ep"], 3)},
+        "ms_per_step_spread": {"min": round(min(r["step_ms"]), 3), "median": round(statistics.median(r["step_ms"]), 3),
+                               "max": round(max(r["step_ms"]), 3),
+                               "source": "events around each timed step, on the launching stream"},
         "ms_per_layer": {k: per_kind[k]["ms_per_launch"] for k in ("weights_ep2tp", "weights_tp2ep", "kv_ep2tp",
                                                                    "kv_tp2ep", "attn_ep2tp", "attn_tp2ep")
                          if k in per_kind},
