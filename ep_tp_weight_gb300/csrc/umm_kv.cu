@@ -313,18 +313,18 @@ __global__ void __launch_bounds__(32) kv_copy_ep2tp_tma(const __grid_constant__ 
 }
 
 // cuTensorMapEncodeTiled, from the driver through the runtime (no link to
-// libcuda); null if the driver does not offer it.
+// libcuda); null if the driver does not offer it.  Looked up once per
+// process; the static's initialisation is thread-safe, so handles used from
+// different host threads may call this at the same time.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool looked = false;
-  if (!looked) {
-    looked = true;
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return nullptr;
+  }();
   return fn;
 }
 

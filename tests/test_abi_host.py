@@ -8,7 +8,6 @@ import ctypes
 import re
 from pathlib import Path
 
-import numpy as np
 import pytest
 
 import oracle
