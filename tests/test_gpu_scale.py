@@ -19,7 +19,7 @@ import oracle
 import synth
 from gpu_helpers import DevUMM, i32
 from helpers import attnslot, heads_of_rank
-from synth.workloads import ATTN_QWEN3_SHAPE, FULL_SWITCH, KV_256REQ, TINY, WEIGHTS_H2048, WEIGHTS_H4096
+from synth.workloads import ATTN_QWEN3_SHAPE, FULL_SWITCH, KV_256REQ, TINY, WEIGHTS_H2048, WEIGHTS_H4096, Workload
 
 pytestmark = pytest.mark.gpu
 
@@ -231,6 +231,16 @@ def _check_kv_tp2ep(run: KVRun, rng):
     np.testing.assert_array_equal(_gather(dev, dst // 2), _expect(dev, src // 2, True))
 
 
+def _group(key: np.ndarray, n: int, a: np.ndarray, b: np.ndarray) -> list:
+    """For each group g < n: (a[key == g], b[key == g]) as device tensors,
+    in token order (one stable sort, then views of one device copy)."""
+    order = np.argsort(key, kind="stable")
+    bounds = np.searchsorted(key[order], np.arange(n + 1))
+    da = torch.from_numpy(np.ascontiguousarray(a[order])).cuda()
+    db = torch.from_numpy(np.ascontiguousarray(b[order])).cuda()
+    return [(da[bounds[g]:bounds[g + 1]], db[bounds[g]:bounds[g + 1]]) for g in range(n)]
+
+
 class KVComplete:
     """Every byte of every KV slot of every region, compared whole.
 
@@ -267,10 +277,8 @@ class KVComplete:
         self.half_u16 = L["pages_tp"] * ps * L["h_tp"] * w.D
         assert self.half_u16 == L["pages_ep"] * ps * w.Hkv * w.D
         self._pin(k, t, o0, o1, src0, tp, dst1, samples)
-        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-        self.by_o0 = {r: (dv(src0[o0 == r]), dv(tp[o0 == r])) for r in range(P)}
-        self.by_move = {(a, b): (dv(src0[(o0 == a) & (o1 == b)]), dv(dst1[(o0 == a) & (o1 == b)]))
-                        for a in range(P) for b in range(P)}
+        self.by_o0 = _group(o0, P, src0, tp)
+        self.by_move = _group(o0 * P + o1, P * P, src0, dst1)
         self.heads = [heads_of_rank(P, w.Hkv, q) for q in range(P)]
 
     def slot_off(self, r: int, s: int) -> int:
@@ -367,16 +375,14 @@ class KVComplete:
         o0, ot = run.owner0[k].astype(np.int64), np.asarray(owner)[k].astype(np.int64)
         src0 = run.ep_pt0[k, p].astype(np.int64) * ps + row
         dst = np.asarray(ep_pt)[k, p].astype(np.int64) * ps + row
-        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-        moves = {(a, b): (dv(src0[(o0 == a) & (ot == b)]), dv(dst[(o0 == a) & (ot == b)]))
-                 for a in range(w.P) for b in range(w.P)}
+        moves = _group(o0 * w.P + ot, w.P * w.P, src0, dst)
         torch.cuda.empty_cache()
         for layer in range(w.N):
             for c in range(2):
                 for a in range(w.P):
                     src = self.initial(a, layer + 1, c).view(-1, w.Hkv, w.D)
                     for b in range(w.P):
-                        s_idx, d_idx = moves[(a, b)]
+                        s_idx, d_idx = moves[a * w.P + b]
                         if len(s_idx):
                             got = self.got(b, layer + 1, c).view(-1, w.Hkv, w.D)[d_idx]
                             assert torch.equal(got, src[s_idx]), ("live", layer, c, a, b)
@@ -394,7 +400,7 @@ class KVComplete:
                 for a in range(w.P):
                     src = self.initial(a, layer + 1, c).view(-1, w.Hkv, w.D)
                     for b in range(w.P):
-                        s_idx, d_idx = self.by_move[(a, b)]
+                        s_idx, d_idx = self.by_move[a * w.P + b]
                         if len(s_idx):
                             exp[b].view(-1, w.Hkv, w.D)[d_idx] = src[s_idx]
                     del src
@@ -443,6 +449,58 @@ def test_kv_and_full_switch_fullsize(w, timed, overlap):
     if w.E:
         _check_weights_round_trip(dev)
     dev.close()
+
+
+# Shapes between the randomised small cases and the two full-size KV
+# workloads: thousands of descriptors on other head/page/rank shapes, each
+# compared byte for byte by KVComplete.  Pools with slack 5 leave the live
+# pages under half the TP pool, so the copies walk the descriptor list
+# instead of the TP-page schedule.
+KV_SHAPES = [
+    Workload("kv_p16_hkv16_d64_ps32", P=16, N=3, Hkv=16, D=64, ps=32, R=600, len_a=1, len_b=4096, slack=1.3),
+    Workload("kv_p4_hkv8_d128", P=4, N=2, Hkv=8, D=128, ps=16, R=500, len_a=1, len_b=8192, slack=1.3),
+    Workload("kv_p8_hkv1_d128_lognormal", P=8, N=2, Hkv=1, D=128, ps=16, R=400, len_kind="lognormal",
+             len_a=1024, len_b=1.0, len_cap=16384, slack=1.3),
+    Workload("kv_p2_hkv2_d72_ps8", P=2, N=3, Hkv=2, D=72, ps=8, R=300, len_a=1, len_b=3000, slack=1.3),
+    Workload("kv_p64_hkv64_d16", P=64, N=2, Hkv=64, D=16, ps=16, R=2000, len_a=1, len_b=1024, slack=1.6),
+    Workload("kv_p8_hkv4_d12_sparse", P=8, N=2, Hkv=4, D=12, ps=16, R=300, len_a=1, len_b=2048, slack=5.0),
+    Workload("kv_p8_hkv4_d128_sparse", P=8, N=2, Hkv=4, D=128, ps=16, R=200, len_a=1, len_b=4096, slack=5.0),
+    Workload("kv_p3_hkv3_d5_ps7", P=3, N=2, Hkv=3, D=5, ps=7, R=200, len_a=1, len_b=500, slack=1.5),
+]
+
+
+@pytest.mark.parametrize("w", KV_SHAPES, ids=lambda w: w.name)
+def test_kv_shapes_complete(w):
+    """EP->TP then TP->EP through the separate entry points; every byte of
+    every KV slot compared after each direction (the TMA or LSU copy the
+    shape selects, in TP-page or descriptor-list order)."""
+    dev = DevUMM(w, seed=w.seed + 7)
+    run = KVRun(dev)
+    full = KVComplete(run, samples=3_000)
+    run.ep2tp()
+    torch.cuda.synchronize()
+    full.check_after_ep2tp()
+    run.tp2ep()
+    torch.cuda.synchronize()
+    full.check_after_tp2ep()
+    dev.close()
+
+
+def test_kv_shapes_take_both_copies_and_both_walks():
+    """The shapes above cover the TMA and the LSU copy, every LSU vector
+    width, and both walks of the copies (TP-page schedule, descriptor list)."""
+    from gpu_helpers import lib_dims
+    kernels, walks = set(), set()
+    for w in KV_SHAPES:
+        k, vb = umm.umm_kv_copy_kernel(lib_dims(w), 0)
+        kernels.add((k, vb))
+        lens = w.lengths()
+        pages_tp = w.pages_tp()
+        most = min(pages_tp, len(lens) * w.max_pages_per_req())
+        walks.add(2 * most >= pages_tp)
+    assert {k for k, _ in kernels} == {umm.UMM_KV_COPY_TMA, umm.UMM_KV_COPY_LSU}
+    assert {vb for k, vb in kernels if k == umm.UMM_KV_COPY_LSU} >= {32, 8, 2}
+    assert walks == {True, False}
 
 
 def test_full_switch_soak_100_round_trips():
