@@ -546,12 +546,12 @@ def run_umm(args, rank, world, local_rank, w=None):
 class CpuSample:
     """The oracle, as it stands, on a bounded sample of the workload: the
     expert weights of every layer EP->TP->EP, and the KV cache of all requests
-    (at most 2048) for one layer EP->TP->EP, three times (greedy placement,
+    (at most 2048) for one layer EP->TP->EP, four times (greedy placement,
     fresh pages each time).  Buffer contents do not change the oracle's speed,
     so they are left as allocated (touched once before timing)."""
 
     KV_REQUESTS = 2048
-    KV_ROUNDS = 3
+    KV_ROUNDS = 4
 
     def __init__(self, w, threads: int, kv_requests: int | None = None, kv_rounds: int | None = None,
                  weight_layers: int | None = None):
