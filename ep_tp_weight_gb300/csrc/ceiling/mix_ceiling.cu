@@ -15,6 +15,9 @@
 // 1 write, sequential; KV EP->TP = shuffled reads, 2 writes (two replicas of
 // each head); KV TP->EP = sequential reads, shuffled writes; attention
 // TP->EP = 1 read, 8 writes (all-gather into every rank's full copy).
+// Cases 7-9 are the other orders KV EP->TP could walk its pages in: each
+// 16 KiB read split into 4 KiB pieces written to shuffled places (the same
+// place in both destinations, as a head's two replicas share a TP page id).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -55,22 +58,28 @@ struct Dsts {
   u256* d[kMaxDst];
 };
 
+// wpiece: vectors per shuffled write piece (kChunkVec: whole 16 KiB chunks;
+// kChunkVec / 4: 4 KiB pieces, wperm then permutes pieces, not chunks)
 __global__ void __launch_bounds__(kT) mix_copy(const u256* src, Dsts dst, int nd, const uint32_t* rperm,
-                                               const uint32_t* wperm, uint32_t nchunks) {
+                                               const uint32_t* wperm, uint32_t wpiece, uint32_t nchunks) {
   const uint32_t b = blockIdx.x;
   if (b >= nchunks) return;
   const uint32_t rc = rperm ? rperm[b] : b;
-  const uint32_t wc = wperm ? wperm[b] : b;
   const u256* s = src + (size_t)rc * kChunkVec;
   u256 v[kU];
+  size_t at[kU];
 #pragma unroll
-  for (int u = 0; u < kU; ++u) v[u] = ld32(s + threadIdx.x + u * kT);
+  for (int u = 0; u < kU; ++u) {
+    const uint32_t i = threadIdx.x + u * kT;   // vector in the chunk
+    v[u] = ld32(s + i);
+    const size_t piece = (size_t)b * (kChunkVec / wpiece) + i / wpiece;
+    at[u] = (wperm ? (size_t)wperm[piece] : piece) * wpiece + i % wpiece;
+  }
 #pragma unroll
   for (int k = 0; k < kMaxDst; ++k) {
     if (k < nd) {
-      u256* o = dst.d[k] + (size_t)wc * kChunkVec;
 #pragma unroll
-      for (int u = 0; u < kU; ++u) st32(o + threadIdx.x + u * kT, v[u]);
+      for (int u = 0; u < kU; ++u) st32(dst.d[k] + at[u], v[u]);
     }
   }
 }
@@ -124,6 +133,7 @@ struct Case {
   int nd;
   bool shuffled_reads, shuffled_writes;
   bool tma = false;      // bulk_copy instead of mix_copy (1R1W sequential only)
+  bool pieces4k = false; // shuffled writes in 4 KiB pieces instead of 16 KiB chunks
 };
 
 }  // namespace
@@ -139,7 +149,7 @@ struct Case {
 
 int main(int argc, char** argv) {
   // argv[1]: GiB per buffer (1..16, default 8); argv[2] (optional): run only
-  // case k of the list below (0..6), allocating only the buffers it uses
+  // case k of the list below (0..9), allocating only the buffers it uses
   const int gib = argc > 1 ? std::max(1, std::min(16, std::atoi(argv[1]))) : 8;
   const int only = argc > 2 ? std::atoi(argv[2]) : -1;
   const size_t S = (size_t)gib << 30;
@@ -149,20 +159,27 @@ int main(int argc, char** argv) {
   uint32_t *rperm = nullptr, *wperm = nullptr;
   CK(cudaMalloc(&src, S));
   CK(cudaMemset(src, 0x5a, S));
-  const int ndst = only == 0 || only == 1 || only == 2 || only == 6 ? 1 : only == 3 || only == 4 ? 2 : kMaxDst;
+  const int ndst = only == 0 || only == 1 || only == 2 || only == 6 ? 1
+                   : only == 3 || only == 4 || only >= 7   ? 2
+                                                          : kMaxDst;
   for (int k = 0; k < ndst; ++k) {
     CK(cudaMalloc(&dst.d[k], S));
     CK(cudaMemset(dst.d[k], 0, S));
   }
-  std::vector<uint32_t> p1(n), p2(n);
+  std::vector<uint32_t> p1(n), p2(n), p3((size_t)n * 4);
   for (uint32_t i = 0; i < n; ++i) p1[i] = p2[i] = i;
+  for (uint32_t i = 0; i < 4 * n; ++i) p3[i] = i;
   std::mt19937_64 rng(20251);
   std::shuffle(p1.begin(), p1.end(), rng);
   std::shuffle(p2.begin(), p2.end(), rng);
+  std::shuffle(p3.begin(), p3.end(), rng);
+  uint32_t* wperm4 = nullptr;
   CK(cudaMalloc(&rperm, (size_t)n * 4));
   CK(cudaMalloc(&wperm, (size_t)n * 4));
+  CK(cudaMalloc(&wperm4, (size_t)n * 16));
   CK(cudaMemcpy(rperm, p1.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
   CK(cudaMemcpy(wperm, p2.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(wperm4, p3.data(), (size_t)n * 16, cudaMemcpyHostToDevice));
   cudaEvent_t e0, e1;
   CK(cudaEventCreate(&e0));
   CK(cudaEventCreate(&e1));
@@ -174,16 +191,20 @@ int main(int argc, char** argv) {
       {"1R2W shuffled reads", "kv_copy_ep2tp", 2, true, false},
       {"1R8W sequential", "attn_kernel TP->EP", 8, false, false},
       {"1R1W sequential, TMA bulk copies", "", 1, false, false, true},
+      {"1R2W shuffled writes", "", 2, false, true},
+      {"1R2W shuffled 4 KiB writes", "", 2, false, true, false, true},
+      {"1R2W shuffled reads, shuffled 4 KiB writes", "", 2, true, true, false, true},
   };
   const int reps = 10;
   for (int ci = 0; ci < (int)(sizeof(cases) / sizeof(cases[0])); ++ci) {
     if (only >= 0 && ci != only) continue;
     const Case& c = cases[ci];
     const uint32_t* rp = c.shuffled_reads ? rperm : nullptr;
-    const uint32_t* wp = c.shuffled_writes ? wperm : nullptr;
+    const uint32_t* wp = c.shuffled_writes ? (c.pieces4k ? wperm4 : wperm) : nullptr;
+    const uint32_t wpiece = c.pieces4k ? (uint32_t)(kChunkVec / 4) : (uint32_t)kChunkVec;
     auto launch = [&]() {
       if (c.tma) bulk_copy<<<n, 32, kChunk + 128>>>(src, dst.d[0], n);
-      else mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, n);
+      else mix_copy<<<n, kT>>>(src, dst, c.nd, rp, wp, wpiece, n);
     };
     for (int w = 0; w < 3; ++w) launch();
     CK(cudaGetLastError());
@@ -203,5 +224,6 @@ int main(int argc, char** argv) {
   CK(cudaFree(src));
   CK(cudaFree(rperm));
   CK(cudaFree(wperm));
+  CK(cudaFree(wperm4));
   return 0;
 }
