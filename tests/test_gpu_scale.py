@@ -486,6 +486,50 @@ def test_kv_shapes_complete(w):
     dev.close()
 
 
+def random_medium_kv(seed: int) -> Workload:
+    """A random KV shape with hundreds of requests and thousands of pages,
+    its pool sized so that the greedy placement's busiest rank fits, and the
+    buffer kept under about 16 GiB."""
+    rng = np.random.default_rng(5000 + seed)
+    P = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16, 32, 64]))
+    if rng.random() < 0.5:
+        divs = [h for h in range(1, P + 1) if P % h == 0]
+        Hkv = int(rng.choice(divs))                          # Hkv <= P: one head per TP rank
+    else:
+        Hkv = P * int(rng.choice([2, 4]))                    # Hkv > P: several heads per TP rank
+    D = int(rng.choice([8, 16, 64, 128, int(rng.integers(1, 160)), int(rng.integers(1, 160))]))
+    ps = int(rng.choice([1, 4, 7, 16, 32, 64]))
+    N = int(rng.integers(1, 4))
+    R = int(rng.integers(50, 800))
+    len_b = int(rng.integers(ps, 400 * ps + 1))
+    w = Workload(f"kv_rand{seed}", P=P, N=N, Hkv=Hkv, D=D, ps=ps, R=R, len_a=0, len_b=len_b, seed=seed)
+    pages = synth.npages(w.lengths(), ps)
+    used, m = max(1, int(pages.sum())), Hkv // w.h_tp
+    bound = used / P + int(pages.max()) + R / P + 1       # busiest rank under the greedy rule
+    slack = max(1.05, 1.02 * m * bound / used) * (5.0 if rng.random() < 0.3 else 1.0)
+    w = w.with_(slack=slack)
+    from gpu_helpers import lib_dims
+    while umm.umm_required_bytes(lib_dims(w)) > (16 << 30) and w.R > 10:
+        w = w.with_(R=w.R // 2)
+    return w
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_kv_random_medium_complete(seed):
+    """Random medium shapes, byte-complete after both directions."""
+    w = random_medium_kv(seed)
+    dev = DevUMM(w, seed=seed)
+    run = KVRun(dev)
+    full = KVComplete(run, samples=1_000)
+    run.ep2tp()
+    torch.cuda.synchronize()
+    full.check_after_ep2tp()
+    run.tp2ep()
+    torch.cuda.synchronize()
+    full.check_after_tp2ep()
+    dev.close()
+
+
 def test_kv_shapes_take_both_copies_and_both_walks():
     """The shapes above cover the TMA and the LSU copy, every LSU vector
     width, and both walks of the copies (TP-page schedule, descriptor list)."""
