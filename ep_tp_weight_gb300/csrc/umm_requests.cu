@@ -10,6 +10,7 @@
 //
 // These kernels are tiny next to the data movement; each runs as one CTA
 // (plus a wide fill for page tables), built on grouped block scans and counts.
+#include <atomic>
 #include <climits>
 
 #include "umm_place.cuh"
@@ -92,16 +93,18 @@ cudaError_t launch_place(const Geo& g, const Ws& w, int32_t R, const int32_t* le
   const int in_smem = need <= 128 * 1024;
   const size_t dyn = in_smem ? need : 0;
   // the shared-memory limit is a per-device function attribute: set it once
-  // per device (calls on one handle come from one host thread)
-  static bool attr_set[kMaxDevices] = {};
+  // per device.  Handles on one device may be driven from different host
+  // threads; setting the same value twice is harmless, so an atomic flag
+  // per device is enough
+  static std::atomic<bool> attr_set[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   place_kernel<<<1, kScanThreads, dyn, s>>>(g, w, R, lens, list_pos, owner, local_pos, in_smem, call);
   return cudaGetLastError();

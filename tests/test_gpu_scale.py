@@ -486,6 +486,43 @@ def test_kv_shapes_complete(w):
     dev.close()
 
 
+@pytest.mark.parametrize("P,R", [(8, 1 << 15), (64, 30_001)])
+def test_kv_many_requests_complete(P, R):
+    """More requests than the other KV tests (2^15, and a ragged 30,001 on 64
+    ranks), short requests (0..12 tokens, pages of 4), through the bench's
+    call sequence.  The sizes stay where the oracle's quadratic request
+    loops (local positions, page hand-out) finish in seconds.  The
+    single-CTA metadata kernels run at that scale:
+      - the request order and the TP page tables equal the oracle's;
+      - the greedy owners, local positions and EP page tables equal it too
+        (the placement sorts its keys in the workspace beyond 16,384
+        requests);
+      - the descriptor list of the EP->TP pass equals the oracle's;
+      - every KV byte is compared after both directions."""
+    w = Workload(f"kv_p{P}_{R}req_u0-12_ps4", P=P, N=1, Hkv=P, D=8, ps=4, R=R, len_a=0, len_b=12, slack=1.3)
+    dev = DevUMM(w, seed=3)
+    run = KVRun(dev)
+    full = KVComplete(run, samples=1_000)
+    L = dev.L
+    nd = int(synth.npages(run.lens, w.ps).sum())
+
+    def descriptors():
+        assert int(dev.buf[L["status_off"] + 8:L["status_off"] + 16].view(torch.int64).item()) == nd
+        return dev.buf[L["desc_off"]:L["desc_off"] + 32 * nd].view(torch.int32).view(nd, 8).cpu().numpy()
+
+    run.ep2tp()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(descriptors(),
+                                  oracle.kv_descriptors(dev.d, 0, run.lens, run.owner0, run.ep_pt0, run.tp_pt))
+    full.check_after_ep2tp()
+    run.tp2ep()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(descriptors(),
+                                  oracle.kv_descriptors(dev.d, 1, run.lens, run.owner1, run.ep_pt1, run.tp_pt))
+    full.check_after_tp2ep()
+    dev.close()
+
+
 def random_medium_kv(seed: int) -> Workload:
     """A random KV shape with hundreds of requests and thousands of pages,
     its pool sized so that the greedy placement's busiest rank fits, and the
