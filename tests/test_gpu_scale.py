@@ -539,15 +539,23 @@ def random_medium_kv(seed: int) -> Workload:
     N = int(rng.integers(1, 4))
     R = int(rng.integers(50, 800))
     len_b = int(rng.integers(ps, 400 * ps + 1))
-    w = Workload(f"kv_rand{seed}", P=P, N=N, Hkv=Hkv, D=D, ps=ps, R=R, len_a=0, len_b=len_b, seed=seed)
-    pages = synth.npages(w.lengths(), ps)
-    used, m = max(1, int(pages.sum())), Hkv // w.h_tp
-    bound = used / P + int(pages.max()) + R / P + 1       # busiest rank under the greedy rule
-    slack = max(1.05, 1.02 * m * bound / used) * (5.0 if rng.random() < 0.3 else 1.0)
-    w = w.with_(slack=slack)
+    sparse = 5.0 if rng.random() < 0.3 else 1.0
+
+    def sized(w: Workload) -> Workload:
+        pages = synth.npages(w.lengths(), w.ps)
+        used, m = max(1, int(pages.sum())), w.Hkv // w.h_tp
+        bound = used / w.P + int(pages.max()) + w.R / w.P + 1   # busiest rank under the greedy rule
+        return w.with_(slack=max(1.05, 1.02 * m * bound / used) * sparse)
+
     from gpu_helpers import lib_dims
-    while umm.umm_required_bytes(lib_dims(w)) > (16 << 30) and w.R > 10:
-        w = w.with_(R=w.R // 2)
+    w = sized(Workload(f"kv_rand{seed}", P=P, N=N, Hkv=Hkv, D=D, ps=ps, R=R, len_a=0, len_b=len_b, seed=seed))
+    while umm.umm_required_bytes(lib_dims(w)) > (16 << 30):
+        if w.R > 10:
+            w = sized(w.with_(R=w.R // 2))
+        elif w.len_b > w.ps:
+            w = sized(w.with_(len_b=max(w.ps, int(w.len_b) // 2)))
+        else:
+            break
     return w
 
 
