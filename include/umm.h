@@ -337,7 +337,8 @@ int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
                      const int32_t* d_tp_page_table, void* stream);
 
 /* Which copy kernel a KV reshard of `dims` launches per layer (host-only;
- * no GPU needed).  dir 0 = EP->TP, 1 = TP->EP.  *kernel = UMM_KV_COPY_TMA
+ * no GPU needed).  The paper has no counterpart: this reports an
+ * implementation choice of this library (§3.2 and §4.3 fix only what moves).  dir 0 = EP->TP, 1 = TP->EP.  *kernel = UMM_KV_COPY_TMA
  * (EP->TP through tensor-map loads and bulk stores, see reshard_kv_ep2tp) or
  * UMM_KV_COPY_LSU (vector loads and stores with 64-bit offsets);
  * *vector_bytes (may be NULL) receives the LSU copy's vector width, 0 for
@@ -350,7 +351,8 @@ int reshard_kv_tp2ep(umm_t* u, int32_t R, int32_t max_pages_per_req, const int32
 int umm_kv_copy_kernel(const umm_dims* dims, int32_t dir, int32_t* kernel, int32_t* vector_bytes);
 
 /* Test hook of the checked build (libumm_checked.so; libumm.so returns
- * UMM_ERR_INVALID_ARG and does nothing).  From the next KV EP->TP call of
+ * UMM_ERR_INVALID_ARG and does nothing).  The paper has no counterpart: it
+ * exercises this library's bounded device wait.  From the next KV EP->TP call of
  * this handle on, every CTA of the TMA copy of layer `layer` makes, once its
  * tensor loads have landed, one more wait on a barrier that never completes,
  * limited to `polls` polls.  That wait runs out and the CTA takes the exit of
