@@ -10,6 +10,7 @@
 //
 // These kernels are tiny next to the data movement; each runs as one CTA
 // (plus a wide fill for page tables), built on grouped block scans and counts.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 
@@ -179,9 +180,10 @@ cudaError_t launch_assign(const Geo& g, const Ws& w, int32_t npools, int32_t R, 
   assign_scan<<<1, kScanThreads, 0, s>>>(g, w, npools, R, maxp, lens, pool, key, free_count, call);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || R == 0) return e;
-  int blocks = (R * 32 + 255) / 256;
-  if (blocks > sms * 8) blocks = sms * 8;
-  assign_emit<<<blocks, 256, 0, s>>>(g, w, R, maxp, lens, pool, free_pages, free_stride, pt);
+  // one warp per request, at most 8 CTAs per SM (64-bit: R * 32 reaches 2^31
+  // at the largest request count)
+  const long long blocks = std::min<long long>(((long long)R * 32 + 255) / 256, (long long)sms * 8);
+  assign_emit<<<(unsigned)blocks, 256, 0, s>>>(g, w, R, maxp, lens, pool, free_pages, free_stride, pt);
   return cudaGetLastError();
 }
 

@@ -210,6 +210,33 @@ def test_empty_and_degenerate_requests():
 
 # ------------------------------------------------------------------ error paths (all-or-nothing)
 
+def test_largest_request_count():
+    """R = 2^26, the most requests a handle accepts, through the single-CTA
+    request-order and page hand-out kernels.  The oracle's definitions are
+    quadratic in R, so the results are checked against what they reduce to
+    here (§3.2 list order, page hand-out in list order): with every request on
+    rank 0 the list position is the request index, and with one-token
+    requests from one pool, request k takes the k-th free page."""
+    R = 1 << 26
+    dims = umm.make_dims(P=1, N=1, ps=16, max_requests=R)
+    nbytes = umm.umm_required_bytes(dims)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    h = umm.umm_create(dims, buf, nbytes)
+    owner = torch.zeros(R, dtype=torch.int32, device="cuda")
+    tp_pos = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    umm.gather_requests_ep2tp(h, R, owner, tp_pos)
+    lens = torch.ones(R, dtype=torch.int32, device="cuda")
+    free = torch.randperm(R, device="cuda", generator=torch.Generator(device="cuda").manual_seed(3)).int()
+    pt = torch.full((R, 1), -2, dtype=torch.int32, device="cuda")
+    umm.umm_assign_pages(h, 1, R, lens, None, None, free, R, R, pt, 1)
+    assert umm.umm_status_sync(h) == (0, 0)
+    assert torch.equal(tp_pos, torch.arange(R, dtype=torch.int32, device="cuda"))
+    assert torch.equal(pt[:, 0], free)
+    umm.umm_destroy(h)
+    del buf, owner, tp_pos, lens, free, pt
+    torch.cuda.empty_cache()
+
+
 def test_kv_device_errors_leave_buffer_untouched():
     w = KV_CASES[1]
     dev = DevUMM(w, seed=2)
