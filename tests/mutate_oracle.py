@@ -109,6 +109,18 @@ MUTATIONS = [
     ("M30", "gate and up rows interleaved instead of in halves", C,
      "    int64_t g = row / Ip;          /* 0 = gate (W1), 1 = up (W3) */\n    int64_t ii = row % Ip;",
      "    int64_t g = row % 2;          /* 0 = gate (W1), 1 = up (W3) */\n    int64_t ii = row / 2;"),
+    ("M31", "KV element map: EP offset ignores the head", C,
+     "(((ep_page * ps + tok_in_page) * Hkv + h) * D + e) * 2",
+     "(((ep_page * ps + tok_in_page) * Hkv + 0) * D + e) * 2"),
+    ("M32", "KV element map: TP offset ignores the local head (Hkv >= 2P)", C,
+     "(((tp_page * ps + tok_in_page) * L[OL_H_TP] + hl) * D + e) * 2",
+     "(((tp_page * ps + tok_in_page) * L[OL_H_TP] + 0) * D + e) * 2"),
+    ("M33", "W2 element map: EP column ignores the TP rank's block", C,
+     "((el * H + h) * I + q * Ip + c) * 2",
+     "((el * H + h) * I + c) * 2"),
+    ("M34", "W13 element map: EP row taken as the TP row", C,
+     "int64_t j = ep_row_of_tp_row(d[OD_W13_SPLIT], I, Ip, q, row);",
+     "int64_t j = row;"),
     ("P1", "policy: a count equal to T_h already switches to EP", POL,
      "want = n > t_high", "want = n >= t_high"),
     ("P2", "policy: a window mean equal to T_l already switches to TP", POL,

@@ -739,3 +739,81 @@ def test_attn_round_trip_and_layer_order(w):
         a = r * L["region_stride"] + L["attnslots_off"] + L["attnslot_stride"]
         b = r * L["region_stride"] + L["attnslots_off"] + (d.N + 1) * L["attnslot_stride"]
         assert np.array_equal(buf[a:b], orig[a:b]), r
+
+
+# ----------------------------------------------------------------------------- element maps
+
+# The element maps (w13_tp_elem, w2_tp_elem, kv_elem) name, for one element,
+# its EP and TP byte offsets; the full-size GPU tests check samples and whole
+# slots through them.  Here they are pinned to the whole-buffer switch
+# functions above (themselves pinned by goldens, equivalence and brute
+# force): on random 16-bit contents, the destination the map names must hold,
+# after the switch, the value at the source it names, for every element.
+
+@pytest.mark.parametrize("split", [0, 1])
+@pytest.mark.parametrize("w", [TINY, SMALL_W], ids=lambda w: w.name)
+def test_weight_element_maps_agree_with_the_switch(w, split):
+    d = dims_of(w, w13_split=split)
+    L = oracle.layout(d)
+    before = fill_regions(L, w.with_(w_sigma=None), seed=11)
+    after = before.copy()
+    oracle.weights_ep2tp(after, d)
+    b16, a16 = before.view(np.uint16), after.view(np.uint16)
+    Ip = d.I // d.P
+    dst_seen = set()
+    for layer in range(d.N):
+        for q in range(d.P):
+            for e in range(d.E):
+                for h in range(d.H):
+                    for row in range(2 * Ip):
+                        s, t = oracle.w13_tp_elem(d, q, e, row, h, layer + 1, layer)
+                        assert a16[t // 2] == b16[s // 2], ("w13", layer, q, e, row, h)
+                        dst_seen.add(t)
+                    for c in range(Ip):
+                        s, t = oracle.w2_tp_elem(d, q, e, h, c, layer + 1, layer)
+                        assert a16[t // 2] == b16[s // 2], ("w2", layer, q, e, h, c)
+                        dst_seen.add(t)
+    # the maps name every TP element once: as many distinct destinations as
+    # TP elements in the N destination slots
+    assert len(dst_seen) == d.N * d.P * d.E * 3 * Ip * d.H
+
+
+@pytest.mark.parametrize("w", [SMALL_KV.with_(kv_sigma=None), SMALL_KV.with_(Hkv=8, D=4, kv_sigma=None),
+                               SMALL_KV.with_(P=8, Hkv=2, D=4, kv_sigma=None)],
+                         ids=["hkv2_p4", "hkv8_p4", "hkv2_p8"])
+def test_kv_element_map_agrees_with_the_switch(w):
+    """EP->TP: every TP replica of every live element holds the value at the
+    EP offset the map names.  TP->EP (greedy owners, new pages): every EP
+    element holds the value at the TP offset (lowest replica) the map names."""
+    d, L, st, buf = _kv_setup(w, seed=4)
+    ep2tp = buf.copy()
+    assert oracle.kv_ep2tp(ep2tp, d, st.lens, st.owner, st.ep_pt, st.tp_pt) == 0
+    owner2, _, _ = oracle.place(d.P, st.lens, key=st.tp_pos)
+    maxp = st.ep_pt.shape[1]
+    _, ep_pt2 = oracle.assign_pages(d.P, st.lens, d.ps, maxp, synth.permutation(9, 4, L["pages_ep"], d.P),
+                                    region=owner2, key=st.tp_pos)
+    tp2ep = ep2tp.copy()
+    assert oracle.kv_tp2ep(tp2ep, d, st.lens, owner2, ep_pt2, st.tp_pt) == 0
+    b16, m16, a16 = buf.view(np.uint16), ep2tp.view(np.uint16), tp2ep.view(np.uint16)
+    checked = 0
+    for k in range(len(st.lens)):
+        for t in range(int(st.lens[k])):
+            p, s = divmod(t, d.ps)
+            for layer in range(d.N):
+                for c in range(2):
+                    for h in range(d.Hkv):
+                        holders = [q for q in range(d.P) if h in heads_of_rank(d.P, d.Hkv, q)]
+                        for e in range(d.D):
+                            for q in holders:
+                                a, b = oracle.kv_elem(d, int(st.owner[k]), q, int(st.ep_pt[k, p]),
+                                                      int(st.tp_pt[k, p]), s, c, h, e, layer + 1, layer)
+                                assert m16[b // 2] == b16[a // 2], ("ep2tp", k, t, layer, c, h, e, q)
+                                checked += 1
+                            a, b = oracle.kv_elem(d, int(owner2[k]), holders[0], int(ep_pt2[k, p]),
+                                                  int(st.tp_pt[k, p]), s, c, h, e, layer + 1, layer)
+                            assert a16[a // 2] == m16[b // 2], ("tp2ep", k, t, layer, c, h, e)
+    assert checked == int(st.lens.sum()) * d.N * 2 * max(d.P, d.Hkv) * d.D
+    # a rank that does not hold the head gets no offsets
+    q_not = next((q for q in range(d.P) if 0 not in heads_of_rank(d.P, d.Hkv, q)), None)
+    if q_not is not None:
+        assert oracle.kv_elem(d, 0, q_not, 0, 0, 0, 0, 0, 0, 1, 0) == (-1, -1)
