@@ -210,6 +210,24 @@ def test_empty_and_degenerate_requests():
 
 # ------------------------------------------------------------------ error paths (all-or-nothing)
 
+@pytest.mark.parametrize("mode,sigma", [(synth.RAW, 1.0), (synth.NORMAL, 1.0), (synth.NORMAL, 0.02)])
+def test_device_generator_equals_host_generator(mode, sigma):
+    """The seeded inputs: the device fill (synth_fill.cu) writes exactly what
+    the host generator defines, element i = value of index base + i, for odd
+    bases and lengths and for a start that is not 16-byte aligned (the
+    kernel's scalar path)."""
+    from gpu_helpers import table_dev
+    out = torch.zeros(1 << 21, dtype=torch.int16, device="cuda")
+    for seed, base, n, skew in ((0, 0, 1 << 20, 0), (7, 12345, 999_997, 1), (1 << 40, 3, 8, 3), (5, 1 << 33, 17, 0)):
+        out.zero_()
+        synth.fill_device(out.data_ptr() + 2 * skew, n, seed, mode, table_dev(sigma).data_ptr() if mode else 0,
+                          base=base)
+        want = synth.fill_host(n, seed, mode, sigma, base=base).view(np.int16)
+        got = out.cpu().numpy()
+        np.testing.assert_array_equal(got[skew:skew + n], want)
+        assert not got[:skew].any() and not got[skew + n:].any()
+
+
 def test_largest_request_count():
     """R = 2^26, the most requests a handle accepts, through the single-CTA
     request-order and page hand-out kernels.  The oracle's definitions are
