@@ -15,7 +15,7 @@ import pytest
 import bench
 import oracle
 import synth
-from helpers import dims_of, initial_kv_state, kvslot, wslot
+from helpers import attnslot, dims_of, initial_kv_state, kvslot, wslot
 from synth.workloads import TINY, Workload
 
 ROOT = Path(__file__).resolve().parent.parent
@@ -148,3 +148,34 @@ def test_configs_cover_the_other_workloads():
     (the line's own value) and the tiny parity case."""
     from synth.workloads import ATTN_QWEN3_SHAPE, KV_256REQ, WEIGHTS_H2048, WEIGHTS_H4096
     assert [w for _, w in bench.OTHER_CONFIGS] == [WEIGHTS_H2048, WEIGHTS_H4096, KV_256REQ, ATTN_QWEN3_SHAPE]
+
+
+@pytest.mark.parametrize("w", [Workload("bytes_attn", P=4, N=1, H=16, Hkv=2, D=8, Hq=8),
+                               Workload("bytes_attn_wide", P=2, N=1, H=8, Hkv=4, D=4, Hq=6)],
+                         ids=lambda w: w.name)
+def test_attention_bytes_equal_elements_the_oracle_moves(w):
+    """Attention weights (memory-saving variant): EP->TP writes every rank's
+    shard once (read once each), TP->EP reads each shard element once (key and
+    value heads from their lowest replica) and writes it into all P full
+    copies; counted from the oracle's writes into zeroed slots."""
+    d = dims_of(w)
+    L = oracle.layout(d)
+    b = bench.algorithmic_bytes(w, [])
+    nfull = ((d.Hq + 2 * d.Hkv) * d.D * d.H + d.H * d.Hq * d.D) * 2        # one full copy, bytes
+    buf = np.zeros(L["ws_off"], dtype=np.uint8)
+    u = buf.view(np.uint16)
+    for r in range(d.P):                                                     # EP layer 0 = slot 1, nonzero
+        a = attnslot(L, r, 1) // 2
+        u[a:a + L["attnslot_stride"] // 2] = 0x3f80
+    oracle.attn_ep2tp(buf, d)
+    written = sum(int(np.count_nonzero(u[attnslot(L, q, 0) // 2:(attnslot(L, q, 0) + L["attnslot_stride"]) // 2]))
+                  for q in range(d.P))
+    assert 2 * 2 * written == b["attn_ep2tp_per_layer"]                     # read + write, 2 B each
+    for r in range(d.P):                                                     # TP -> EP into zeroed EP slots
+        a = attnslot(L, r, 1) // 2
+        u[a:a + L["attnslot_stride"] // 2] = 0
+    oracle.attn_tp2ep(buf, d)
+    written2 = sum(int(np.count_nonzero(u[attnslot(L, r, 1) // 2:(attnslot(L, r, 1) + L["attnslot_stride"]) // 2]))
+                   for r in range(d.P))
+    assert 2 * written2 == d.P * nfull
+    assert b["attn_tp2ep_per_layer"] == nfull + 2 * written2
