@@ -328,16 +328,40 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Shared memory a block gets without an opt-in, static and dynamic together.
+constexpr uint64_t kDefaultSmemPerBlock = 48 * 1024;
+// The TMA copy's static shared memory: its mbarriers, rounded up to the
+// 1024-byte alignment of the tile array that follows (ptxas reports 1024
+// bytes).  The launcher checks the kernel's real figure before each launch.
+constexpr uint64_t kTmaStaticSmem = 1024;
+
 // Whether the shape lets KV EP->TP run through kv_copy_ep2tp_tma: one head
 // per TP rank (Hkv <= P), a head row a multiple of 16 bytes (bulk-copy
-// sizes), boxes of at most 256 per dimension, the tiles within the default
-// 48 KiB of shared memory, and every tensor coordinate below 2^31.
+// sizes), boxes of at most 256 per dimension, the tiles (plus 128 bytes to
+// align them, plus the static part) within the 48 KiB a block gets without
+// an opt-in, and every tensor coordinate below 2^31.
 bool ep2tp_tma_shape(const Geo& g) {
   const uint64_t tile = (uint64_t)g.ps * (uint64_t)g.D * 2;
   const uint64_t stride = (tile + 127) / 128 * 128;
   const uint64_t smem = (uint64_t)g.Hkv * stride;
-  return g.Hkv >= 1 && g.Hkv <= g.P && g.D <= 256 && g.ps <= 256 && (g.D * 2) % 16 == 0 && smem + 128 <= 48 * 1024 &&
-         g.pages_ep >= 1 && g.pages_ep <= 0x7fffffffll && g.P <= 0x7fffffff;
+  return g.Hkv >= 1 && g.Hkv <= g.P && g.D <= 256 && g.ps <= 256 && (g.D * 2) % 16 == 0 &&
+         smem + 128 + kTmaStaticSmem <= kDefaultSmemPerBlock && g.pages_ep >= 1 && g.pages_ep <= 0x7fffffffll &&
+         g.P <= 0x7fffffff;
+}
+
+// The TMA copy's static shared memory as the runtime reports it (looked up
+// once; the initialisation of the static is thread-safe), or ~0 if the
+// lookup fails, which sends every shape to the LSU copy.
+uint64_t tma_static_smem() {
+  static const uint64_t bytes = []() -> uint64_t {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kv_copy_ep2tp_tma) != cudaSuccess) {
+      cudaGetLastError();
+      return ~0ull;
+    }
+    return (uint64_t)fa.sharedSizeBytes;
+  }();
+  return bytes;
 }
 
 // Launches the TMA copy for one layer when the shape allows it; *done = false
@@ -349,6 +373,8 @@ cudaError_t launch_ep2tp_tma(const Geo& g, const KVParams& p, int layer, int64_t
   const uint64_t tile = (uint64_t)g.ps * (uint64_t)g.D * 2;
   const uint64_t stride = (tile + 127) / 128 * 128;
   const uint64_t smem = (uint64_t)g.Hkv * stride;
+  const uint64_t stat = tma_static_smem();
+  if (stat > kDefaultSmemPerBlock || smem + 128 + stat > kDefaultSmemPerBlock) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaSuccess;
   // the EP view of layer `layer` in every region, one map per half (K, V):

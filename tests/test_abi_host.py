@@ -319,6 +319,15 @@ def test_page_ids_are_capped_below_2_31(umm):
     (4, 4, 256, 32, ("LSU", 32)),     # 4 heads x 16 KiB tiles: over 48 KiB of shared memory
     (8, 1, 128, 512, ("LSU", 32)),    # a 512-row page: over the 256 box limit
     (3, 1, 5, 16, ("LSU", 2)),
+    # tiles + 128 B alignment room + 1 KiB static shared memory within 48 KiB:
+    (2, 1, 128, 187, ("TMA", 0)),     # 187 rows x 256 B = 47,872 B: 49,024 B in all, fits
+    (2, 1, 128, 188, ("LSU", 32)),    # 188 rows: 49,280 B, over
+    (2, 2, 128, 93, ("TMA", 0)),      # two heads of 93 rows: 47,616 B of tiles, fits
+    (2, 2, 128, 94, ("LSU", 32)),
+    (2, 1, 256, 16, ("TMA", 0)),      # head of 256 elements: the box limit
+    (2, 1, 264, 16, ("LSU", 16)),     # 264: over it
+    (2, 1, 8, 256, ("TMA", 0)),       # 256-row page: the box limit
+    (2, 1, 8, 257, ("LSU", 16)),
 ])
 def test_kv_copy_kernel_choice(umm, P, Hkv, D, ps, want):
     d = _kv_dims(umm, P, Hkv, D, ps, 64 * max(1, Hkv // max(1, Hkv // P)))

@@ -99,6 +99,25 @@ def test_kv_full_buffer_parity(w):
     dev.close()
 
 
+# Shapes at the limits of the TMA copy (one head per TP rank): the largest
+# tiles that fit its 48 KiB of shared memory, and boxes of 256 elements and of
+# 256 rows (the tensor-map box limit).  Whole buffers against the oracle.
+TMA_EDGE_CASES = [
+    Workload("kv_tma_tile_187rows_d128", P=2, N=2, Hkv=1, D=128, ps=187, R=5, len_a=1, len_b=600),
+    Workload("kv_tma_two_heads_93rows_d128", P=2, N=2, Hkv=2, D=128, ps=93, R=5, len_a=1, len_b=400),
+    Workload("kv_tma_head_256", P=2, N=2, Hkv=1, D=256, ps=16, R=6, len_a=1, len_b=90),
+    Workload("kv_tma_page_256rows", P=2, N=2, Hkv=1, D=8, ps=256, R=6, len_a=1, len_b=1200),
+]
+
+
+@pytest.mark.parametrize("w", TMA_EDGE_CASES, ids=lambda w: w.name)
+def test_kv_tma_edge_shapes(w):
+    dev = DevUMM(w, seed=6)
+    assert umm.umm_kv_copy_kernel(dev.dims, 0) == (umm.UMM_KV_COPY_TMA, 0)
+    _kv_round(dev, w)
+    dev.close()
+
+
 def test_weights_and_kv_together_and_modes():
     w = TINY
     dev = DevUMM(w, seed=9)
