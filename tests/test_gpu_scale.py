@@ -123,6 +123,27 @@ def test_weights_fullsize(w):
     dev.close()
 
 
+@pytest.mark.parametrize("I", [10912, 10922], ids=["vec16", "vec2"])
+def test_weights_largest_region(I):
+    """The largest expert-weight region the handle accepts: 2 ranks, one expert
+    each, H = 65,536, 3*I*H just under 2^31 - 2^16 elements per region (the
+    bound that keeps the kernel's 32-bit vector indices and exact divisions
+    valid), 16 GiB.  I = 10,912 runs 16-byte vectors; I = 10,922 (I/P odd)
+    2-byte ones, whose highest vector index is 2,147,352,575.  Sampled oracle
+    maps, whole-layer torch slices, then the round trip over every slot."""
+    w = Workload(f"weights_p2_e2_h65536_i{I}_1layer", P=2, N=1, E=2, H=65536, I=I)
+    dev = DevUMM(w, seed=17)
+    rng = np.random.default_rng(I)
+    umm.reshard_weights_ep2tp(dev.h)
+    torch.cuda.synchronize()
+    assert dev.status() == (0, 0)
+    _check_weights_ep2tp(dev, rng)
+    umm.reshard_weights_tp2ep(dev.h)
+    torch.cuda.synchronize()
+    _check_weights_round_trip(dev)
+    dev.close()
+
+
 # ------------------------------------------------------------------ KV, in the bench's call sequence
 
 class KVRun:
